@@ -1,0 +1,156 @@
+"""CPU oracle for the stable LSD radix sort -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the bench's ``cpu_baseline`` /
+``--impl reference`` legs may import this package.  The CUDA library never
+does, and the two share no code.  The arithmetic lives in ``oracle.c`` (plain,
+single-threaded C, compiled on first use with the host C compiler); this file
+only marshals numpy arrays.
+
+Functions:
+  sort(key_type, keys, values=None, begin_bit=0, end_bit=None, radix_bits=8)
+      LSD radix sort by counting-sort passes ("Radix sort を実装 & 測定してみた",
+      section アルゴリズムの詳細; "Radix sort paralelo sobre el scan", section
+      Las tres fases de una pasada).
+  one_bit_split_sort(...)
+      the one-bit index-formula sort of "Radix sort を実装 & 測定してみた",
+      section アルゴリズムの詳細, as an independent second path.
+  decimal_lsd_trace(keys, passes)
+      the base-10 worked example of "Radix sort paralelo sobre el scan",
+      section La idea y el requisito de estabilidad.
+  ordered_keys(key_type, keys)
+      the order-preserving unsigned map ("Radix sort を実装 & 測定してみた",
+      section 符号付型、浮動小数点型に対する radix sort, for float32; "Radix sort
+      paralelo sobre el scan", section Claves con signo y en coma flotante, for
+      int32).
+  exclusive_scan(values)
+      the exclusive prefix sum ("高性能计算：GPU上的基数排序", section CPU上的扫描).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIBDIR = os.path.join(_HERE, "_lib")
+_LIB = os.path.join(_LIBDIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+KEY_TYPES = {"u32": 0, "i32": 1, "f32": 2, "u64": 3}
+KEY_DTYPE = {"u32": np.uint32, "i32": np.uint32, "f32": np.uint32, "u64": np.uint64}
+KEY_BITS = {"u32": 32, "i32": 32, "f32": 32, "u64": 64}
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into a shared library (host C compiler, -O2, no vectorisation flags)."""
+    with _lock:
+        if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+            os.makedirs(_LIBDIR, exist_ok=True)
+            tmp = _LIB + f".{os.getpid()}.tmp"
+            subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC])
+            os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _bind(lib):
+    vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    lib.oracle_lsd_sort.argtypes = [i32, vp, vp, vp, vp, sz, i32, i32, i32]
+    lib.oracle_lsd_sort.restype = i32
+    lib.oracle_one_bit_split_sort.argtypes = [i32, vp, vp, vp, vp, sz, i32, i32]
+    lib.oracle_one_bit_split_sort.restype = i32
+    lib.oracle_decimal_lsd_trace.argtypes = [vp, sz, i32, vp]
+    lib.oracle_decimal_lsd_trace.restype = i32
+    lib.oracle_ordered_keys.argtypes = [i32, vp, sz, vp]
+    lib.oracle_ordered_keys.restype = None
+    lib.oracle_exclusive_scan.argtypes = [vp, vp, sz]
+    lib.oracle_exclusive_scan.restype = None
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        _lib = _bind(ctypes.CDLL(_LIB))
+    return _lib
+
+
+def _as_keys(key_type: str, keys) -> np.ndarray:
+    dt = KEY_DTYPE[key_type]
+    a = np.ascontiguousarray(keys)
+    if a.dtype.itemsize != np.dtype(dt).itemsize:
+        raise TypeError(f"{key_type} keys need {np.dtype(dt).itemsize}-byte elements, got {a.dtype}")
+    return a.view(dt)
+
+
+def _vp(a):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def sort(key_type: str, keys, values=None, begin_bit: int = 0, end_bit: int | None = None,
+         radix_bits: int = 8, lib=None):
+    """Stable LSD radix sort; returns (keys_out, values_out or None) as new arrays."""
+    k = _as_keys(key_type, keys)
+    end_bit = KEY_BITS[key_type] if end_bit is None else end_bit
+    n = k.size
+    ko = np.empty_like(k)
+    vi = None if values is None else np.ascontiguousarray(values, dtype=np.uint32)
+    vo = None if vi is None else np.empty_like(vi)
+    if vi is not None and vi.size != n:
+        raise ValueError("values must match keys in length")
+    rc = (lib or _load()).oracle_lsd_sort(KEY_TYPES[key_type], _vp(k), _vp(ko), _vp(vi), _vp(vo), n,
+                                 begin_bit, end_bit, radix_bits)
+    if rc != 0:
+        raise ValueError(f"oracle_lsd_sort failed with code {rc}")
+    return ko, vo
+
+
+def one_bit_split_sort(key_type: str, keys, values=None, begin_bit: int = 0,
+                       end_bit: int | None = None, lib=None):
+    """The one-bit index-formula sort, one pass per bit of [begin_bit, end_bit)."""
+    k = _as_keys(key_type, keys)
+    end_bit = KEY_BITS[key_type] if end_bit is None else end_bit
+    n = k.size
+    ko = np.empty_like(k)
+    vi = None if values is None else np.ascontiguousarray(values, dtype=np.uint32)
+    vo = None if vi is None else np.empty_like(vi)
+    rc = (lib or _load()).oracle_one_bit_split_sort(KEY_TYPES[key_type], _vp(k), _vp(ko), _vp(vi), _vp(vo),
+                                           n, begin_bit, end_bit)
+    if rc != 0:
+        raise ValueError(f"oracle_one_bit_split_sort failed with code {rc}")
+    return ko, vo
+
+
+def decimal_lsd_trace(keys, passes: int, lib=None) -> np.ndarray:
+    """Array after each base-10 LSD pass, shape (passes, n)."""
+    k = np.ascontiguousarray(keys, dtype=np.uint64)
+    out = np.empty((passes, k.size), dtype=np.uint64)
+    rc = (lib or _load()).oracle_decimal_lsd_trace(_vp(k), k.size, passes, _vp(out))
+    if rc != 0:
+        raise ValueError(f"oracle_decimal_lsd_trace failed with code {rc}")
+    return out
+
+
+def ordered_keys(key_type: str, keys, lib=None) -> np.ndarray:
+    """The order-preserving unsigned key of every element (uint64 array)."""
+    k = _as_keys(key_type, keys)
+    out = np.empty(k.size, dtype=np.uint64)
+    (lib or _load()).oracle_ordered_keys(KEY_TYPES[key_type], _vp(k), k.size, _vp(out))
+    return out
+
+
+def exclusive_scan(values, lib=None) -> np.ndarray:
+    v = np.ascontiguousarray(values, dtype=np.uint64)
+    out = np.empty_like(v)
+    (lib or _load()).oracle_exclusive_scan(_vp(v), _vp(out), v.size)
+    return out
+
+
+def load_variant(path: str):
+    """Bind a separately compiled copy of oracle.c (the tests plant mistakes in copies)."""
+    return _bind(ctypes.CDLL(path))
