@@ -1,0 +1,405 @@
+#!/usr/bin/env python3
+"""Throughput of the GB300 LSD radix sort on its headline workload.
+
+One step = one whole sort (every digit pass, through the C ABI) of 2^28
+uniform uint32 keys, keys only, bits [0, 32), with the keys already resident
+in HBM.  Prints ONE JSON line (rank 0):
+
+  value      Gkeys/s over all ranks (each rank sorts its own replica: the sort
+             does not shard, so N GPUs run N independent sorts, weak scaling)
+  roofline   the dominant kernel's algorithmic bytes per launch / its average
+             CUDA-event duration, against the measured HBM copy bandwidth
+  e2e        the same metric through rs_sort_host with pinned host buffers,
+             host->device and device->host copies inside the timed region
+  cpu_baseline  the CPU oracle (single thread) on a bounded sample
+
+`--impl reference` times the CPU oracle itself as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Gkeys/s sorted (32-bit keys, 2^28) on 1 GB300; % of HBM roofline"
+DEFAULT_WORKLOAD = "c4a_u32_2p28"
+L2_BYTES = 126 * 2**20
+FALLBACK_HBM_GBS = 6800.0
+KIND_NAMES = {1: "histogram", 2: "onesweep_pass", 3: "upsweep", 4: "spine_scan", 5: "downsweep",
+              6: "copy"}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--log2n", type=int, default=None, help="override the size (uniform u32 sweep)")
+    ap.add_argument("--algo", default="auto", choices=["auto", "onesweep", "reduce_scan"])
+    ap.add_argument("--radix-bits", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return ws, rank, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, x: float, device) -> float:
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "lsd_radix_sort_key_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kind: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if its kernel
+    sources are the ones built now; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        data = json.load(f)
+    entry = data.get(f"{kind}:{workload}")
+    if not entry or entry.get("source_hash") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        mhz, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                mhz.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not mhz:
+            return None
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(maxes) if maxes else None,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+def cpu_baseline(workload, key_type, begin_bit, end_bit, log2n, budget_s=10.0):
+    """The CPU oracle (one thread) on a bounded sample of the same workload."""
+    import oracle
+    import synth
+    sample_log2 = min(log2n, 24)
+    n = 1 << sample_log2
+    keys = workload.keys(n) if log2n is None or workload.log2n == log2n else synth.u32_uniform(n, 1)
+    vals = workload.values(n)
+    oracle.sort(key_type, keys[:1024], None if vals is None else vals[:1024], begin_bit, end_bit)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.sort(key_type, keys, vals, begin_bit, end_bit)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 50:
+            break
+    return {"value": round(n * reps / el / 1e9, 6), "unit": "Gkeys/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{reps} x oracle sort of the first 2^{sample_log2} keys of the workload "
+                      f"({el:.1f} s single-threaded C counting-sort LSD, r=8)"}
+
+
+# --------------------------------------------------------------- reference
+
+def run_reference(args):
+    ws, rank, local, pg = dist_setup(args)
+    if rank != 0:
+        return
+    import synth
+    import oracle
+    w = synth.WORKLOADS[args.workload] if args.log2n is None else synth.sweep_workload(args.log2n)
+    sample_log2 = min(w.log2n, 22)
+    n = 1 << sample_log2
+    keys = w.keys(n)
+    vals = w.values(n)
+    for _ in range(args.warmup):
+        oracle.sort(w.key_type, keys, vals, w.begin_bit, w.end_bit)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.sort(w.key_type, keys, vals, w.begin_bit, w.end_bit)
+    el = time.perf_counter() - t0
+    value = n * args.steps / el / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "Gkeys/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.key_type, "data": "synthetic",
+            "config": {"workload": w.name, "n": w.n, "sample_n": n, "key_type": w.key_type,
+                       "begin_bit": w.begin_bit, "end_bit": w.end_bit,
+                       "values": w.with_values},
+            "cpu_baseline": {"value": round(value, 6), "unit": "Gkeys/s", "cores": 1,
+                             "kind": "oracle",
+                             "sample": f"each step sorts the first 2^{sample_log2} keys of the "
+                                       "workload with the single-threaded CPU oracle"},
+            "e2e": {"value": round(value, 6), "unit": "Gkeys/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------- ours
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import lsd_radix_sort_key_gb300 as rs
+    import synth
+
+    ws, rank, local, pg = dist_setup(args)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    rs.lib()
+
+    w = synth.WORKLOADS[args.workload] if args.log2n is None else synth.sweep_workload(args.log2n)
+    kt, n, b, e = w.key_type, w.n, w.begin_bit, w.end_bit
+    kbytes = rs.KEY_BYTES[kt]
+    tdt = torch.int64 if kbytes == 8 else torch.int32
+    # Each rank sorts its own replica (seed offset by rank): no data-path exchange.
+    host_k = torch.empty(n, dtype=tdt).pin_memory()
+    import dataclasses
+    wr = dataclasses.replace(w, seed=w.seed + (rank << 40))
+    wr.keys(out=host_k.numpy().view(np.uint64 if kbytes == 8 else np.uint32))
+    host_v = None
+    if w.with_values:
+        host_v = torch.empty(n, dtype=torch.int32).pin_memory()
+        synth.iota_u32(n, out=host_v.numpy().view(np.uint32))
+    kin = host_k.to(dev)
+    vin = host_v.to(dev) if host_v is not None else None
+    kout = torch.empty_like(kin)
+    vout = torch.empty_like(vin) if vin is not None else None
+    tb = rs.rs_temp_bytes(kt, w.with_values, n, b, e)
+    temp = torch.empty(tb, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    desc = rs.make_desc(kt, kin, kout, vin, vout, n, b, e, temp, tb, stream, args.algo,
+                        args.radix_bits)
+    nk = rs.rs_sort_kernel_count(desc)
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+    step_events = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+                   for _ in range(args.steps)]
+
+    for _ in range(max(args.warmup, 3)):
+        st, kinds = rs.rs_sort_profiled(desc, events)
+        assert st == 0, rs.STATUS.get(st)
+    torch.cuda.synchronize(dev)
+    status = rs.rs_device_status(temp, stream)
+    assert status == 0, rs.STATUS.get(status)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(pg)
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for s in range(args.steps):
+        st, kinds = rs.rs_sort_profiled(desc, step_events[s])
+        assert st == 0
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(pg)
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(end)
+    total_ms = max_over_ranks(pg, total_ms, dev)
+    status = rs.rs_device_status(temp, stream)
+    assert status == 0, rs.STATUS.get(status)
+
+    # Per-kernel durations inside the timed region.
+    per_kind = {}
+    for s in range(args.steps):
+        ev = step_events[s]
+        for i, k in enumerate(kinds):
+            per_kind.setdefault(k, []).append(ev[i].elapsed_time(ev[i + 1]))
+    ms_per_step = total_ms / args.steps
+    value = n * ws / (ms_per_step * 1e-3) / 1e9
+
+    peaks, peak_src = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    vbytes = 4 if w.with_values else 0
+    passes = -(-(e - b) // (args.radix_bits or 8)) if e > b else 0
+    # algorithmic bytes per launch of each kernel kind
+    algo_bytes = {1: n * kbytes, 2: n * 2 * (kbytes + vbytes), 3: n * kbytes, 4: 0,
+                  5: n * (kbytes + 2 * (kbytes + vbytes)) - n * kbytes}
+    dominant = max(per_kind, key=lambda k: sum(per_kind[k]))
+    dom_ms = statistics.mean(per_kind[dominant])
+    dom_bytes = algo_bytes[dominant]
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    kernels = {KIND_NAMES[k]: {"launches_per_step": len(v) // args.steps,
+                               "avg_ms": round(statistics.mean(v), 4),
+                               "share": round(sum(v) / sum(sum(x) for x in per_kind.values()), 4)}
+               for k, v in per_kind.items()}
+    resolved = args.algo if args.algo != "auto" else ("onesweep" if n < (1 << 30) else "reduce_scan")
+    scheme_bpk = ((kbytes if resolved == "onesweep" else passes * kbytes)
+                  + passes * 2 * (kbytes + vbytes))
+    ideal_bpk = passes * 2 * (kbytes + vbytes)
+    sort_gbs = n * scheme_bpk / (ms_per_step * 1e-3) / 1e9
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "Gkeys/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": kt,
+        "data": "synthetic",
+        "config": {"workload": w.name, "n": n, "key_type": kt, "begin_bit": b, "end_bit": e,
+                   "values": w.with_values, "algo": resolved, "radix_bits": args.radix_bits or 8,
+                   "passes": passes, "parallelism": f"replicas x{ws}",
+                   "l2": "inputs larger than L2 (no flush needed)" if n * kbytes > L2_BYTES
+                   else "inputs fit in L2 (no flush: L2-resident number)"},
+        "roofline": {"bound": "hbm", "kernel": KIND_NAMES[dominant],
+                     "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "peak_source": peak_src,
+                     "traffic": ncu_traffic(KIND_NAMES[dominant], w.name),
+                     "algorithmic_bytes_per_launch": dom_bytes,
+                     "avg_launch_ms": round(dom_ms, 4)},
+        "sort_roofline": {"scheme": resolved, "bytes_per_key": scheme_bpk,
+                          "ideal_bytes_per_key": ideal_bpk,
+                          "achieved_gbs": round(sort_gbs, 1),
+                          "frac_scheme": round(sort_gbs / hbm, 4),
+                          "frac_ideal": round(n * ideal_bpk / (ms_per_step * 1e-3) / 1e9 / hbm, 4)},
+        "kernels": kernels,
+        "gpu_launches": nk * args.steps,
+        "clocks": clk,
+    }
+
+    # End to end through the C ABI with host buffers.
+    if not args.no_e2e:
+        host_ko = torch.empty_like(host_k).pin_memory()
+        host_vo = torch.empty_like(host_v).pin_memory() if host_v is not None else None
+        del kout, vout, kin, vin
+        wb = rs.rs_host_work_bytes(kt, w.with_values, n, b, e)
+        del temp
+        torch.cuda.empty_cache()
+        work = torch.empty(wb, dtype=torch.uint8, device=dev)
+        for _ in range(2):
+            assert rs.rs_sort_host(kt, host_k, host_ko, host_v, host_vo, n, b, e, work, wb,
+                                   stream) == 0
+        torch.cuda.synchronize(dev)
+        e2e_steps = max(3, min(args.steps, 10))
+        barrier(pg)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(e2e_steps):
+            assert rs.rs_sort_host(kt, host_k, host_ko, host_v, host_vo, n, b, e, work, wb,
+                                   stream) == 0
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(pg, s0.elapsed_time(s1), dev) / e2e_steps
+        line["e2e"] = {"value": round(n * ws / (e2e_ms * 1e-3) / 1e9, 3), "unit": "Gkeys/s",
+                       "h2d_bytes_per_step": n * (kbytes + vbytes),
+                       "d2h_bytes_per_step": n * (kbytes + vbytes),
+                       "ms_per_step": round(e2e_ms, 3), "steps": e2e_steps,
+                       "api": "rs_sort_host (pinned host buffers)"}
+        del work
+
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(w, kt, b, e, w.log2n)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

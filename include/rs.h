@@ -1,0 +1,207 @@
+/*
+ * rs.h -- C ABI of a stable least-significant-digit radix sort for NVIDIA
+ * GB300 (sm_103a).
+ *
+ * What is computed.  For n keys of one type (uint32, int32, float32 or
+ * uint64) and a bit range [begin_bit, end_bit), the sort returns the keys,
+ * and optionally one uint32 value per key, in the unique STABLE order of
+ *     D(i) = bits [begin_bit, end_bit) of T(key_i),
+ * ascending, ties kept in input order.  T is the order-preserving map to an
+ * unsigned integer:
+ *   - uint32, uint64: identity;
+ *   - int32: flip the sign bit ("Radix sort paralelo sobre el scan", section
+ *     "Claves con signo y en coma flotante");
+ *   - float32: NaN (any payload, either sign) and +-Inf map to 0xFFFFFFFF;
+ *     otherwise a set sign bit flips every bit and a clear one sets the MSB
+ *     ("Radix sort を実装 & 測定してみた", section "符号付型、浮動小数点型に
+ *     対する radix sort").  So -Inf, +Inf and all NaNs tie after every finite
+ *     value, in input order, and -0.0 sorts just before +0.0.
+ * The output keys are the ORIGINAL bit patterns (nothing is re-encoded).  Bits
+ * outside [begin_bit, end_bit) of T(key) do not influence the order.
+ *
+ * Method.  Each pass sorts by one r-bit digit (r = 8 by default, 4 on
+ * request), lowest digit first ("Radix sort paralelo sobre el scan", sections
+ * "La idea y el requisito de estabilidad" and "Las tres fases de una pasada"):
+ * a per-block digit histogram, an exclusive scan of the block counts laid out
+ * digit-major, a block-local stable rank and shuffle in shared memory, and a
+ * coalesced scatter ("정렬: 라딕스와 머지소트", 13.3-13.6).  Two schedules
+ * exist: a three-kernel reduce-then-scan per pass, and a single-pass chained
+ * scan with decoupled look-back that reads every key once up front for all
+ * pass histograms.
+ *
+ * Conventions for every entry point below.
+ *   Pointers.  Key, value and temp pointers are DEVICE pointers (cudaMalloc,
+ *     cudaMallocAsync or a framework allocator) unless a parameter says
+ *     "host".  The caller owns all memory; the library allocates no device
+ *     memory and keeps no device state outside `temp`.
+ *   Alignment.  Keys and values must be aligned to their element size; temp
+ *     must be 256-byte aligned.  16-byte-aligned keys take the vector-load
+ *     path; others are still sorted correctly.
+ *   Aliasing.  keys_out may equal keys_in exactly (in-place sort; an odd pass
+ *     count then costs one extra copy), likewise vals_out and vals_in.  Any
+ *     other overlap among the key, value and temp buffers is RS_ERR_ALIAS.
+ *   Stream.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *     default stream).  Calls only enqueue work: they do not synchronise,
+ *     allocate or read device memory back, so they may be captured into a
+ *     CUDA graph.  RS_OK means "enqueued"; faults the device detects (a
+ *     look-back wait that ran out, an index that failed its bounds check) are
+ *     written to an error word inside `temp` and read by rs_device_status().
+ *   Sizes.  n may be 0 (nothing is launched).  n must be at most
+ *     2^32 - 2^16 (the chained-scan schedule needs n < 2^30 and AUTO falls
+ *     back to reduce-then-scan above that).  0 <= begin_bit <= end_bit <= 32 (64 for
+ *     uint64); begin_bit == end_bit is a stable copy.
+ *   Errors.  Invalid arguments return an error before anything is enqueued;
+ *     RS_ERR_CUDA reports a failed launch or copy (cudaGetLastError).
+ */
+#ifndef RS_H
+#define RS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rs_status {
+    RS_OK = 0,
+    RS_ERR_INVALID_ARG = 1,    /* null pointer, bad bit range, n too large, bad enum   */
+    RS_ERR_TEMP_TOO_SMALL = 2, /* temp_bytes < rs_temp_bytes(...)                      */
+    RS_ERR_ALIAS = 3,          /* partially overlapping buffers                        */
+    RS_ERR_CUDA = 4,           /* a CUDA runtime call failed                           */
+    RS_ERR_DEVICE_TIMEOUT = 5, /* a look-back wait ran out (device error word)         */
+    RS_ERR_CHECK_FAILED = 6,   /* a device bounds check failed (device error word)     */
+    RS_ERR_UNSUPPORTED = 7     /* valid request this build does not handle             */
+} rs_status;
+
+typedef enum rs_key_type { RS_U32 = 0, RS_I32 = 1, RS_F32 = 2, RS_U64 = 3 } rs_key_type;
+
+typedef enum rs_algo {
+    RS_ALGO_AUTO = 0,        /* chained scan when n < 2^30, else reduce-then-scan   */
+    RS_ALGO_ONESWEEP = 1,    /* one upfront histogram read + one kernel per pass    */
+    RS_ALGO_REDUCE_SCAN = 2  /* upsweep + spine scan + downsweep per pass           */
+} rs_algo;
+
+/*
+ * Bytes of device scratch ("temp") a sort of this shape needs, for every
+ * schedule and digit width, so one temp buffer serves any rs_sort variant.
+ * Pure host arithmetic: needs no GPU and never fails (0 for n == 0).
+ * Returns (size_t)-1 for arguments every sort would reject.
+ */
+size_t rs_temp_bytes(rs_key_type key_type, int with_values, size_t n, int begin_bit, int end_bit);
+
+/* Keys only.  keys_in: n keys (read only); keys_out: n keys (written). */
+rs_status rs_sort_keys_u32(const uint32_t* keys_in, uint32_t* keys_out, size_t n,
+                           int begin_bit, int end_bit, void* temp, size_t temp_bytes, void* stream);
+rs_status rs_sort_keys_i32(const int32_t* keys_in, int32_t* keys_out, size_t n,
+                           int begin_bit, int end_bit, void* temp, size_t temp_bytes, void* stream);
+rs_status rs_sort_keys_f32(const float* keys_in, float* keys_out, size_t n,
+                           int begin_bit, int end_bit, void* temp, size_t temp_bytes, void* stream);
+rs_status rs_sort_keys_u64(const uint64_t* keys_in, uint64_t* keys_out, size_t n,
+                           int begin_bit, int end_bit, void* temp, size_t temp_bytes, void* stream);
+
+/* Keys with one uint32 value each ("Radix sort paralelo sobre el scan": the
+ * payload travels with its key).  vals_in / vals_out: n values. */
+rs_status rs_sort_pairs_u32(const uint32_t* keys_in, uint32_t* keys_out, const uint32_t* vals_in,
+                            uint32_t* vals_out, size_t n, int begin_bit, int end_bit,
+                            void* temp, size_t temp_bytes, void* stream);
+rs_status rs_sort_pairs_i32(const int32_t* keys_in, int32_t* keys_out, const uint32_t* vals_in,
+                            uint32_t* vals_out, size_t n, int begin_bit, int end_bit,
+                            void* temp, size_t temp_bytes, void* stream);
+rs_status rs_sort_pairs_f32(const float* keys_in, float* keys_out, const uint32_t* vals_in,
+                            uint32_t* vals_out, size_t n, int begin_bit, int end_bit,
+                            void* temp, size_t temp_bytes, void* stream);
+rs_status rs_sort_pairs_u64(const uint64_t* keys_in, uint64_t* keys_out, const uint32_t* vals_in,
+                            uint32_t* vals_out, size_t n, int begin_bit, int end_bit,
+                            void* temp, size_t temp_bytes, void* stream);
+
+/*
+ * The general entry point: every typed call above fills one of these.  Fields
+ * have the meanings given in the conventions; vals_in / vals_out are both NULL
+ * for a keys-only sort.
+ */
+typedef struct rs_sort_desc {
+    rs_key_type key_type;
+    const void* keys_in;
+    void* keys_out;
+    const uint32_t* vals_in;
+    uint32_t* vals_out;
+    size_t n;
+    int begin_bit;
+    int end_bit;
+    rs_algo algo;       /* schedule, RS_ALGO_AUTO by default                    */
+    int radix_bits;     /* digit width: 0 = default (8), or 4 or 8              */
+    void* temp;
+    size_t temp_bytes;
+    void* stream;
+    /* Testing hooks, 0 in normal use.  spin_limit bounds each look-back wait
+     * (0 = the default bound, about a second).  stall_tile = t + 1 makes tile
+     * t of the chained-scan schedule never publish its digit counts, so the
+     * waits behind it run out and the sort reports RS_ERR_DEVICE_TIMEOUT. */
+    uint32_t spin_limit;
+    int32_t stall_tile;
+} rs_sort_desc;
+
+rs_status rs_sort(const rs_sort_desc* desc);
+
+/*
+ * As rs_sort, and records CUDA events around every kernel: events[0] before
+ * the first launch and events[i] after the i-th, on desc->stream.  `events`
+ * holds max_events cudaEvent_t handles (as void*) created by the caller.  On
+ * return *num_kernels is the number of kernels launched and kinds[i] (if
+ * kinds != NULL, max_events entries) names kernel i+1's role:
+ *   1 histogram (all passes), 2 chained-scan pass, 3 upsweep, 4 spine scan,
+ *   5 downsweep, 6 copy.
+ * Returns RS_ERR_INVALID_ARG if max_events is smaller than kernels + 1.
+ */
+rs_status rs_sort_profiled(const rs_sort_desc* desc, void* const* events, int max_events,
+                           int* num_kernels, int* kinds);
+
+/*
+ * Number of kernels rs_sort would launch for this descriptor (no launch).
+ * Returns -1 for a descriptor rs_sort would reject.
+ */
+int rs_sort_kernel_count(const rs_sort_desc* desc);
+
+/*
+ * Waits for `stream`, then reads and clears the device error word in `temp`
+ * (the last sort enqueued with this temp on this stream).  Returns RS_OK,
+ * RS_ERR_DEVICE_TIMEOUT, RS_ERR_CHECK_FAILED, or RS_ERR_CUDA if the wait or
+ * the copy fails.  This is the only entry point that synchronises.
+ */
+rs_status rs_device_status(const void* temp, void* stream);
+
+/* Static English text for a status code; never NULL. */
+const char* rs_status_string(rs_status status);
+
+/*
+ * CUDA graph of one whole sort.  rs_graph_create captures rs_sort(desc) on
+ * desc->stream (which must not be capturing already) and instantiates it;
+ * the graph bakes in every pointer and size of `desc`.  rs_graph_launch
+ * replays it on `stream`.  The graph object is host memory owned by the
+ * caller until rs_graph_destroy.
+ */
+typedef struct rs_graph rs_graph;
+rs_status rs_graph_create(const rs_sort_desc* desc, rs_graph** graph);
+rs_status rs_graph_launch(const rs_graph* graph, void* stream);
+void rs_graph_destroy(rs_graph* graph);
+
+/*
+ * End-to-end sort of HOST buffers.  h_keys_in / h_vals_in (host, read only,
+ * page-locked for full copy speed) are copied to the device, sorted, and the
+ * result copied to h_keys_out / h_vals_out (host), all enqueued on `stream`.
+ * d_work is a caller-owned device buffer of rs_host_work_bytes(...) bytes
+ * holding the device copies and the sort's temp.  The call returns once the
+ * work is enqueued; the host outputs are valid after the stream completes.
+ */
+size_t rs_host_work_bytes(rs_key_type key_type, int with_values, size_t n, int begin_bit,
+                          int end_bit);
+rs_status rs_sort_host(rs_key_type key_type, const void* h_keys_in, void* h_keys_out,
+                       const uint32_t* h_vals_in, uint32_t* h_vals_out, size_t n, int begin_bit,
+                       int end_bit, void* d_work, size_t work_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RS_H */

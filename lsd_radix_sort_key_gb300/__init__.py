@@ -1,0 +1,255 @@
+"""Python binding of the GB300 LSD radix sort (C ABI in include/rs.h).
+
+Argument marshalling only: every step of the sort runs in the CUDA library
+``_lib/librs.so``.  PyTorch supplies device memory and streams.  If the
+library has not been built this module raises on first use -- there is no
+fallback.
+
+Low-level functions carry the C names (``rs_sort_keys_u32``, ``rs_sort_pairs_f32``,
+``rs_temp_bytes``, ``rs_sort``, ...) and accept torch tensors or raw integer
+addresses for pointers.  ``sort()`` is the convenience wrapper that allocates
+outputs and temp with torch.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+KEY_TYPES = {"u32": 0, "i32": 1, "f32": 2, "u64": 3}
+KEY_BYTES = {"u32": 4, "i32": 4, "f32": 4, "u64": 8}
+KEY_BITS = {"u32": 32, "i32": 32, "f32": 32, "u64": 64}
+ALGOS = {"auto": 0, "onesweep": 1, "reduce_scan": 2}
+STATUS = {0: "RS_OK", 1: "RS_ERR_INVALID_ARG", 2: "RS_ERR_TEMP_TOO_SMALL", 3: "RS_ERR_ALIAS",
+          4: "RS_ERR_CUDA", 5: "RS_ERR_DEVICE_TIMEOUT", 6: "RS_ERR_CHECK_FAILED",
+          7: "RS_ERR_UNSUPPORTED"}
+KERNEL_KINDS = {1: "histogram", 2: "onesweep_pass", 3: "upsweep", 4: "spine_scan",
+                5: "downsweep", 6: "copy"}
+LIB_PATH = _build.LIB
+
+
+class RadixSortError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)}")
+
+
+class SortDesc(ctypes.Structure):
+    """Mirror of rs_sort_desc."""
+    _fields_ = [("key_type", ctypes.c_int), ("keys_in", ctypes.c_void_p),
+                ("keys_out", ctypes.c_void_p), ("vals_in", ctypes.c_void_p),
+                ("vals_out", ctypes.c_void_p), ("n", ctypes.c_size_t),
+                ("begin_bit", ctypes.c_int), ("end_bit", ctypes.c_int), ("algo", ctypes.c_int),
+                ("radix_bits", ctypes.c_int), ("temp", ctypes.c_void_p),
+                ("temp_bytes", ctypes.c_size_t), ("stream", ctypes.c_void_p),
+                ("spin_limit", ctypes.c_uint32), ("stall_tile", ctypes.c_int32)]
+
+
+_lib = None
+
+# C signatures of every exported symbol (name -> (restype, argtypes)).
+_vp, _sz, _i, _u32p = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p
+_KEYS_SIG = (_i, [_vp, _vp, _sz, _i, _i, _vp, _sz, _vp])
+_PAIRS_SIG = (_i, [_vp, _vp, _vp, _vp, _sz, _i, _i, _vp, _sz, _vp])
+SIGNATURES = {
+    "rs_temp_bytes": (_sz, [_i, _i, _sz, _i, _i]),
+    "rs_sort": (_i, [ctypes.POINTER(SortDesc)]),
+    "rs_sort_profiled": (_i, [ctypes.POINTER(SortDesc), ctypes.POINTER(_vp), _i,
+                              ctypes.POINTER(_i), ctypes.POINTER(_i)]),
+    "rs_sort_kernel_count": (_i, [ctypes.POINTER(SortDesc)]),
+    "rs_device_status": (_i, [_vp, _vp]),
+    "rs_status_string": (ctypes.c_char_p, [_i]),
+    "rs_graph_create": (_i, [ctypes.POINTER(SortDesc), ctypes.POINTER(_vp)]),
+    "rs_graph_launch": (_i, [_vp, _vp]),
+    "rs_graph_destroy": (None, [_vp]),
+    "rs_host_work_bytes": (_sz, [_i, _i, _sz, _i, _i]),
+    "rs_sort_host": (_i, [_i, _vp, _vp, _vp, _vp, _sz, _i, _i, _vp, _sz, _vp]),
+}
+for _t in ("u32", "i32", "f32", "u64"):
+    SIGNATURES[f"rs_sort_keys_{_t}"] = _KEYS_SIG
+    SIGNATURES[f"rs_sort_pairs_{_t}"] = _PAIRS_SIG
+
+
+def build(force: bool = False) -> str:
+    return _build.build(force=force)
+
+
+def lib():
+    """The loaded CUDA library; raises if it was never built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library {LIB_PATH} is missing: run __graft_entry__.build() "
+                               "(or python -m lsd_radix_sort_key_gb300._build) first")
+        h = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(h, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = h
+    return _lib
+
+
+def _addr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise RadixSortError(code, where)
+
+
+# ---------------------------------------------------------- C-named wrappers
+
+def rs_temp_bytes(key_type: str, with_values: bool, n: int, begin_bit: int, end_bit: int) -> int:
+    return lib().rs_temp_bytes(KEY_TYPES[key_type], int(bool(with_values)), n, begin_bit, end_bit)
+
+
+def rs_host_work_bytes(key_type: str, with_values: bool, n: int, begin_bit: int, end_bit: int) -> int:
+    return lib().rs_host_work_bytes(KEY_TYPES[key_type], int(bool(with_values)), n, begin_bit, end_bit)
+
+
+def rs_status_string(code: int) -> str:
+    return lib().rs_status_string(code).decode()
+
+
+def _typed(name):
+    def keys_fn(keys_in, keys_out, n, begin_bit, end_bit, temp, temp_bytes, stream=None):
+        return getattr(lib(), f"rs_sort_keys_{name}")(
+            _addr(keys_in), _addr(keys_out), n, begin_bit, end_bit, _addr(temp), temp_bytes,
+            _stream(stream))
+
+    def pairs_fn(keys_in, keys_out, vals_in, vals_out, n, begin_bit, end_bit, temp, temp_bytes,
+                 stream=None):
+        return getattr(lib(), f"rs_sort_pairs_{name}")(
+            _addr(keys_in), _addr(keys_out), _addr(vals_in), _addr(vals_out), n, begin_bit,
+            end_bit, _addr(temp), temp_bytes, _stream(stream))
+
+    keys_fn.__name__ = f"rs_sort_keys_{name}"
+    pairs_fn.__name__ = f"rs_sort_pairs_{name}"
+    return keys_fn, pairs_fn
+
+
+rs_sort_keys_u32, rs_sort_pairs_u32 = _typed("u32")
+rs_sort_keys_i32, rs_sort_pairs_i32 = _typed("i32")
+rs_sort_keys_f32, rs_sort_pairs_f32 = _typed("f32")
+rs_sort_keys_u64, rs_sort_pairs_u64 = _typed("u64")
+
+
+def make_desc(key_type, keys_in, keys_out, vals_in, vals_out, n, begin_bit, end_bit, temp,
+              temp_bytes, stream=None, algo="auto", radix_bits=0, spin_limit=0, stall_tile=0):
+    return SortDesc(KEY_TYPES[key_type], _addr(keys_in), _addr(keys_out), _addr(vals_in),
+                    _addr(vals_out), n, begin_bit, end_bit, ALGOS[algo], radix_bits, _addr(temp),
+                    temp_bytes, _stream(stream), spin_limit, stall_tile)
+
+
+def rs_sort(desc: SortDesc) -> int:
+    return lib().rs_sort(ctypes.byref(desc))
+
+
+def rs_sort_kernel_count(desc: SortDesc) -> int:
+    return lib().rs_sort_kernel_count(ctypes.byref(desc))
+
+
+def rs_sort_profiled(desc: SortDesc, events):
+    """events: list of torch.cuda.Event(enable_timing=True); returns (status, kinds)."""
+    for e in events:
+        if e.cuda_event == 0:
+            # torch creates events lazily; record once on the stream to create them
+            e.record()
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    nk = ctypes.c_int(0)
+    kinds = (ctypes.c_int * len(events))()
+    st = lib().rs_sort_profiled(ctypes.byref(desc), arr, len(events), ctypes.byref(nk), kinds)
+    return st, [kinds[i] for i in range(nk.value)]
+
+
+def rs_device_status(temp, stream=None) -> int:
+    return lib().rs_device_status(_addr(temp), _stream(stream))
+
+
+def rs_sort_host(key_type, h_keys_in, h_keys_out, h_vals_in, h_vals_out, n, begin_bit, end_bit,
+                 d_work, work_bytes, stream=None) -> int:
+    return lib().rs_sort_host(KEY_TYPES[key_type], _addr(h_keys_in), _addr(h_keys_out),
+                              _addr(h_vals_in), _addr(h_vals_out), n, begin_bit, end_bit,
+                              _addr(d_work), work_bytes, _stream(stream))
+
+
+class Graph:
+    """A captured, instantiated CUDA graph of one whole sort (rs_graph_*)."""
+
+    def __init__(self, desc: SortDesc):
+        h = ctypes.c_void_p()
+        _check(lib().rs_graph_create(ctypes.byref(desc), ctypes.byref(h)), "rs_graph_create")
+        self._h = h
+
+    def launch(self, stream=None):
+        _check(lib().rs_graph_launch(self._h, _stream(stream)), "rs_graph_launch")
+
+    def close(self):
+        if self._h:
+            lib().rs_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# --------------------------------------------------------------- convenience
+
+def key_type_of(t) -> str:
+    import torch
+    m = {torch.int32: "i32", torch.float32: "f32"}
+    for name in ("uint32", "uint64"):
+        dt = getattr(torch, name, None)
+        if dt is not None:
+            m[dt] = "u" + name[4:]
+    if t.dtype not in m:
+        raise TypeError(f"pass key_type= for keys of dtype {t.dtype}")
+    return m[t.dtype]
+
+
+def sort(keys, values=None, *, key_type=None, begin_bit=0, end_bit=None, algo="auto",
+         radix_bits=0, keys_out=None, values_out=None, temp=None, stream=None):
+    """Stable radix sort of a CUDA tensor of keys (and uint32 values).
+
+    Returns (keys_out, values_out or None).  Allocates the outputs and temp
+    with torch when they are not given; enqueues on `stream` (default: the
+    current stream) and does not synchronise.
+    """
+    import torch
+    kt = key_type or key_type_of(keys)
+    if keys.element_size() != KEY_BYTES[kt] or not keys.is_contiguous() or not keys.is_cuda:
+        raise ValueError("keys must be a contiguous CUDA tensor with elements of the key size")
+    n = keys.numel()
+    end_bit = KEY_BITS[kt] if end_bit is None else end_bit
+    if keys_out is None:
+        keys_out = torch.empty_like(keys)
+    if values is not None and values_out is None:
+        values_out = torch.empty_like(values)
+    tb = rs_temp_bytes(kt, values is not None, n, begin_bit, end_bit)
+    if tb == ctypes.c_size_t(-1).value:
+        raise RadixSortError(1, "rs_temp_bytes")
+    if temp is None:
+        temp = torch.empty(max(tb, 1), dtype=torch.uint8, device=keys.device)
+    desc = make_desc(kt, keys, keys_out, values, values_out, n, begin_bit, end_bit, temp,
+                     temp.numel(), stream, algo, radix_bits)
+    _check(rs_sort(desc), "rs_sort")
+    return keys_out, values_out

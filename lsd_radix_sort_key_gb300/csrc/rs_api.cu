@@ -1,0 +1,388 @@
+// rs_api.cu -- the extern "C" boundary declared in include/rs.h: argument
+// checks, the temp layout, schedule choice, profiling events, CUDA graphs and
+// the host-buffer path.  The kernels live in rs_kernels.cuh and are
+// instantiated per key type in rs_sort_<type>.cu.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <new>
+
+#include "rs.h"
+#include "rs_config.h"
+#include "rs_kernels.cuh"
+
+// Instantiated in rs_sort_<type>.cu; not here.
+namespace rs {
+extern template rs_status run_sort<KU32>(Plan& pl);
+extern template rs_status run_sort<KI32>(Plan& pl);
+extern template rs_status run_sort<KF32>(Plan& pl);
+extern template rs_status run_sort<KU64>(Plan& pl);
+}  // namespace rs
+
+namespace {
+
+constexpr size_t kMaxN = (size_t)0xFFFF0000u;        // 2^32 - 2^16
+constexpr size_t kOnesweepMaxN = ((size_t)1 << 30) - 1;
+constexpr uint32_t kDefaultSpinLimit = 1u << 20;      // each spin is one L2 round trip (~1 s in all)
+
+int key_bytes(rs_key_type kt) { return kt == RS_U64 ? 8 : 4; }
+int key_bits(rs_key_type kt) { return kt == RS_U64 ? 64 : 32; }
+bool valid_kt(int kt) { return kt >= RS_U32 && kt <= RS_U64; }
+
+bool ranges_overlap(const void* a, size_t abytes, const void* b, size_t bbytes)
+{
+    if (!a || !b || abytes == 0 || bbytes == 0) return false;
+    uintptr_t a0 = (uintptr_t)a, a1 = a0 + abytes, b0 = (uintptr_t)b, b1 = b0 + bbytes;
+    return a0 < b1 && b0 < a1;
+}
+
+rs_status check_shape(rs_key_type kt, size_t n, int begin_bit, int end_bit)
+{
+    if (!valid_kt(kt)) return RS_ERR_INVALID_ARG;
+    if (n > kMaxN) return RS_ERR_INVALID_ARG;
+    if (begin_bit < 0 || end_bit < begin_bit || end_bit > key_bits(kt)) return RS_ERR_INVALID_ARG;
+    return RS_OK;
+}
+
+// Validates a descriptor and resolves it into a Plan (no CUDA call).
+rs_status make_plan(const rs_sort_desc* d, rs::Plan* pl)
+{
+    if (!d) return RS_ERR_INVALID_ARG;
+    rs_status st = check_shape(d->key_type, d->n, d->begin_bit, d->end_bit);
+    if (st != RS_OK) return st;
+    const bool vals = d->vals_in != nullptr || d->vals_out != nullptr;
+    if (vals && (!d->vals_in || !d->vals_out)) return RS_ERR_INVALID_ARG;
+    if (d->radix_bits != 0 && d->radix_bits != 4 && d->radix_bits != 8) return RS_ERR_INVALID_ARG;
+    if (d->algo != RS_ALGO_AUTO && d->algo != RS_ALGO_ONESWEEP && d->algo != RS_ALGO_REDUCE_SCAN)
+        return RS_ERR_INVALID_ARG;
+    if (d->stall_tile < 0) return RS_ERR_INVALID_ARG;
+    const size_t n = d->n;
+    const int kb = key_bytes(d->key_type);
+    *pl = rs::Plan{};
+    pl->kt = d->key_type;
+    pl->vals = vals;
+    pl->n = n;
+    pl->begin_bit = d->begin_bit;
+    pl->end_bit = d->end_bit;
+    pl->radix_bits = d->radix_bits == 0 ? 8 : d->radix_bits;
+    pl->passes = rs::passes_for(d->begin_bit, d->end_bit, pl->radix_bits);
+    pl->algo = d->algo;
+    if (pl->algo == RS_ALGO_AUTO) pl->algo = n <= kOnesweepMaxN ? RS_ALGO_ONESWEEP : RS_ALGO_REDUCE_SCAN;
+    if (pl->algo == RS_ALGO_ONESWEEP && n > kOnesweepMaxN) return RS_ERR_UNSUPPORTED;
+    pl->keys_in = d->keys_in;
+    pl->keys_out = d->keys_out;
+    pl->vals_in = d->vals_in;
+    pl->vals_out = d->vals_out;
+    pl->temp = static_cast<unsigned char*>(d->temp);
+    pl->stream = static_cast<cudaStream_t>(d->stream);
+    pl->spin_limit = d->spin_limit ? d->spin_limit : kDefaultSpinLimit;
+    pl->stall_tile = d->stall_tile;
+    if (n == 0) return RS_OK;
+
+    if (!d->keys_in || !d->keys_out || !d->temp) return RS_ERR_INVALID_ARG;
+    if ((uintptr_t)d->keys_in % kb || (uintptr_t)d->keys_out % kb) return RS_ERR_INVALID_ARG;
+    if (vals && ((uintptr_t)d->vals_in % 4 || (uintptr_t)d->vals_out % 4)) return RS_ERR_INVALID_ARG;
+    if ((uintptr_t)d->temp % 256) return RS_ERR_INVALID_ARG;
+    pl->lay = rs::temp_layout(kb, vals, n, d->begin_bit, d->end_bit);
+    if (d->temp_bytes < pl->lay.total) return RS_ERR_TEMP_TOO_SMALL;
+
+    // Aliasing: exact in-place is allowed; any other overlap is rejected.
+    const size_t kbytes = n * kb, vbytes = n * 4;
+    const void* bufs[5] = {d->keys_in, d->keys_out, d->vals_in, d->vals_out, d->temp};
+    const size_t sizes[5] = {kbytes, kbytes, vals ? vbytes : 0, vals ? vbytes : 0, pl->lay.total};
+    for (int i = 0; i < 5; ++i)
+        for (int j = i + 1; j < 5; ++j) {
+            const bool same_exact = bufs[i] == bufs[j] && sizes[i] == sizes[j];
+            const bool allowed = same_exact && ((i == 0 && j == 1) || (i == 2 && j == 3));
+            if (!allowed && ranges_overlap(bufs[i], sizes[i], bufs[j], sizes[j])) return RS_ERR_ALIAS;
+        }
+    if (vals && (d->keys_in == d->keys_out) != (d->vals_in == d->vals_out)) return RS_ERR_ALIAS;
+    return RS_OK;
+}
+
+rs_status dispatch(rs::Plan& pl)
+{
+    switch (pl.kt) {
+    case RS_U32: return rs::run_sort<rs::KU32>(pl);
+    case RS_I32: return rs::run_sort<rs::KI32>(pl);
+    case RS_F32: return rs::run_sort<rs::KF32>(pl);
+    default:     return rs::run_sort<rs::KU64>(pl);
+    }
+}
+
+// Enqueue a whole sort described by `pl` (already validated).
+rs_status enqueue(rs::Plan& pl)
+{
+    if (pl.n == 0) return RS_OK;
+    if (pl.count_only) {
+        if (pl.passes == 0) { pl.launched = 0; return RS_OK; }
+        return dispatch(pl);
+    }
+    // Clear the error word, the tile tickets and the global histograms.
+    if (cudaMemsetAsync(pl.temp + pl.lay.meta, 0, rs::kMetaWords * 4, pl.stream) != cudaSuccess)
+        return RS_ERR_CUDA;
+    if (pl.passes == 0) {  // empty bit range: a stable sort is the identity
+        if (pl.keys_out != pl.keys_in &&
+            cudaMemcpyAsync(pl.keys_out, pl.keys_in, pl.n * key_bytes((rs_key_type)pl.kt),
+                            cudaMemcpyDeviceToDevice, pl.stream) != cudaSuccess)
+            return RS_ERR_CUDA;
+        if (pl.vals && pl.vals_out != pl.vals_in &&
+            cudaMemcpyAsync(pl.vals_out, pl.vals_in, pl.n * 4, cudaMemcpyDeviceToDevice, pl.stream) !=
+                cudaSuccess)
+            return RS_ERR_CUDA;
+        return cudaGetLastError() == cudaSuccess ? RS_OK : RS_ERR_CUDA;
+    }
+    return dispatch(pl);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t rs_temp_bytes(rs_key_type key_type, int with_values, size_t n, int begin_bit, int end_bit)
+{
+    if (check_shape(key_type, n, begin_bit, end_bit) != RS_OK) return (size_t)-1;
+    if (n == 0) return 0;
+    return rs::temp_layout(key_bytes(key_type), with_values != 0, n, begin_bit, end_bit).total;
+}
+
+rs_status rs_sort(const rs_sort_desc* desc)
+{
+    rs::Plan pl;
+    rs_status st = make_plan(desc, &pl);
+    if (st != RS_OK) return st;
+    return enqueue(pl);
+}
+
+int rs_sort_kernel_count(const rs_sort_desc* desc)
+{
+    if (!desc) return -1;
+    // The count depends on the shape only: stand in distinct, never
+    // dereferenced addresses for any missing buffer so the checks pass.
+    rs_sort_desc d = *desc;
+    const bool vals = d.vals_in || d.vals_out;
+    if (!d.keys_in) d.keys_in = reinterpret_cast<const void*>((uintptr_t)1 << 40);
+    if (!d.keys_out) d.keys_out = reinterpret_cast<void*>((uintptr_t)2 << 40);
+    if (vals && !d.vals_in) d.vals_in = reinterpret_cast<const uint32_t*>((uintptr_t)3 << 40);
+    if (vals && !d.vals_out) d.vals_out = reinterpret_cast<uint32_t*>((uintptr_t)4 << 40);
+    if (!d.temp) {
+        d.temp = reinterpret_cast<void*>((uintptr_t)5 << 40);
+        d.temp_bytes = (size_t)1 << 40;
+    }
+    rs::Plan pl;
+    if (make_plan(&d, &pl) != RS_OK) return -1;
+    pl.count_only = true;
+    if (enqueue(pl) != RS_OK) return -1;
+    return pl.launched;
+}
+
+rs_status rs_sort_profiled(const rs_sort_desc* desc, void* const* events, int max_events,
+                           int* num_kernels, int* kinds)
+{
+    if (!events || !num_kernels) return RS_ERR_INVALID_ARG;
+    int need = rs_sort_kernel_count(desc);
+    if (need < 0) return RS_ERR_INVALID_ARG;
+    if (max_events < need + 1) return RS_ERR_INVALID_ARG;
+    rs::Plan pl;
+    rs_status st = make_plan(desc, &pl);
+    if (st != RS_OK) return st;
+    pl.events = reinterpret_cast<cudaEvent_t const*>(events);
+    pl.max_events = max_events;
+    pl.kinds = kinds;
+    if (cudaEventRecord(pl.events[0], pl.stream) != cudaSuccess) return RS_ERR_CUDA;
+    st = enqueue(pl);
+    *num_kernels = pl.launched;
+    return st;
+}
+
+#define RS_TYPED(NAME, KT, KTYPE)                                                                   \
+    rs_status rs_sort_keys_##NAME(const KTYPE* keys_in, KTYPE* keys_out, size_t n, int begin_bit,   \
+                                  int end_bit, void* temp, size_t temp_bytes, void* stream)         \
+    {                                                                                               \
+        rs_sort_desc d{};                                                                           \
+        d.key_type = KT;                                                                            \
+        d.keys_in = keys_in;                                                                        \
+        d.keys_out = keys_out;                                                                      \
+        d.n = n;                                                                                    \
+        d.begin_bit = begin_bit;                                                                    \
+        d.end_bit = end_bit;                                                                        \
+        d.temp = temp;                                                                              \
+        d.temp_bytes = temp_bytes;                                                                  \
+        d.stream = stream;                                                                          \
+        return rs_sort(&d);                                                                         \
+    }                                                                                               \
+    rs_status rs_sort_pairs_##NAME(const KTYPE* keys_in, KTYPE* keys_out, const uint32_t* vals_in,  \
+                                   uint32_t* vals_out, size_t n, int begin_bit, int end_bit,        \
+                                   void* temp, size_t temp_bytes, void* stream)                     \
+    {                                                                                               \
+        if (n > 0 && (!vals_in || !vals_out)) return RS_ERR_INVALID_ARG;                            \
+        rs_sort_desc d{};                                                                           \
+        d.key_type = KT;                                                                            \
+        d.keys_in = keys_in;                                                                        \
+        d.keys_out = keys_out;                                                                      \
+        d.vals_in = vals_in;                                                                        \
+        d.vals_out = vals_out;                                                                      \
+        d.n = n;                                                                                    \
+        d.begin_bit = begin_bit;                                                                    \
+        d.end_bit = end_bit;                                                                        \
+        d.temp = temp;                                                                              \
+        d.temp_bytes = temp_bytes;                                                                  \
+        d.stream = stream;                                                                          \
+        return rs_sort(&d);                                                                         \
+    }
+
+RS_TYPED(u32, RS_U32, uint32_t)
+RS_TYPED(i32, RS_I32, int32_t)
+RS_TYPED(f32, RS_F32, float)
+RS_TYPED(u64, RS_U64, uint64_t)
+#undef RS_TYPED
+
+rs_status rs_device_status(const void* temp, void* stream)
+{
+    if (!temp) return RS_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t* err = reinterpret_cast<uint32_t*>(const_cast<void*>(temp)) + rs::kErrWord;
+    uint32_t word = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return RS_ERR_CUDA;
+    if (cudaMemcpyAsync(&word, err, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess) return RS_ERR_CUDA;
+    if (cudaMemsetAsync(err, 0, 4, s) != cudaSuccess) return RS_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return RS_ERR_CUDA;
+    if (word & (1u << RS_ERR_DEVICE_TIMEOUT)) return RS_ERR_DEVICE_TIMEOUT;
+    if (word) return RS_ERR_CHECK_FAILED;
+    return RS_OK;
+}
+
+const char* rs_status_string(rs_status status)
+{
+    switch (status) {
+    case RS_OK: return "ok";
+    case RS_ERR_INVALID_ARG: return "invalid argument";
+    case RS_ERR_TEMP_TOO_SMALL: return "temp buffer smaller than rs_temp_bytes()";
+    case RS_ERR_ALIAS: return "buffers overlap";
+    case RS_ERR_CUDA: return "CUDA runtime call failed";
+    case RS_ERR_DEVICE_TIMEOUT: return "device look-back wait ran out";
+    case RS_ERR_CHECK_FAILED: return "device bounds check failed";
+    case RS_ERR_UNSUPPORTED: return "unsupported request";
+    }
+    return "unknown status";
+}
+
+struct rs_graph {
+    cudaGraph_t graph;
+    cudaGraphExec_t exec;
+};
+
+rs_status rs_graph_create(const rs_sort_desc* desc, rs_graph** graph)
+{
+    if (!desc || !graph) return RS_ERR_INVALID_ARG;
+    *graph = nullptr;
+    rs::Plan pl;
+    rs_status st = make_plan(desc, &pl);
+    if (st != RS_OK) return st;
+    cudaStream_t cap = nullptr;
+    if (cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking) != cudaSuccess) return RS_ERR_CUDA;
+    pl.stream = cap;
+    rs_graph g{nullptr, nullptr};
+    if (cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        cudaStreamDestroy(cap);
+        return RS_ERR_CUDA;
+    }
+    st = enqueue(pl);
+    cudaError_t e = cudaStreamEndCapture(cap, &g.graph);
+    cudaStreamDestroy(cap);
+    if (st != RS_OK || e != cudaSuccess) {
+        if (g.graph) cudaGraphDestroy(g.graph);
+        return st != RS_OK ? st : RS_ERR_CUDA;
+    }
+    if (cudaGraphInstantiate(&g.exec, g.graph, 0) != cudaSuccess) {
+        cudaGraphDestroy(g.graph);
+        return RS_ERR_CUDA;
+    }
+    rs_graph* out = new (std::nothrow) rs_graph(g);
+    if (!out) {
+        cudaGraphExecDestroy(g.exec);
+        cudaGraphDestroy(g.graph);
+        return RS_ERR_CUDA;
+    }
+    *graph = out;
+    return RS_OK;
+}
+
+rs_status rs_graph_launch(const rs_graph* graph, void* stream)
+{
+    if (!graph) return RS_ERR_INVALID_ARG;
+    return cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)) == cudaSuccess ? RS_OK
+                                                                                          : RS_ERR_CUDA;
+}
+
+void rs_graph_destroy(rs_graph* graph)
+{
+    if (!graph) return;
+    cudaGraphExecDestroy(graph->exec);
+    cudaGraphDestroy(graph->graph);
+    delete graph;
+}
+
+// Host path work buffer: [temp][keys in][keys out][vals in][vals out].
+static rs::TempLayout host_work_layout(rs_key_type kt, bool vals, size_t n, int begin_bit, int end_bit,
+                                       size_t* kin, size_t* kout, size_t* vin, size_t* vout)
+{
+    rs::TempLayout t = rs::temp_layout(key_bytes(kt), vals, n, begin_bit, end_bit);
+    size_t off = t.total;
+    const size_t kb = rs::align_up(n * key_bytes(kt), 256), vb = vals ? rs::align_up(n * 4, 256) : 0;
+    *kin = off; off += kb;
+    *kout = off; off += kb;
+    *vin = off; off += vb;
+    *vout = off; off += vb;
+    t.total = off;  // whole work buffer
+    return t;
+}
+
+size_t rs_host_work_bytes(rs_key_type key_type, int with_values, size_t n, int begin_bit, int end_bit)
+{
+    if (check_shape(key_type, n, begin_bit, end_bit) != RS_OK) return (size_t)-1;
+    if (n == 0) return 0;
+    size_t a, b, c, d;
+    return host_work_layout(key_type, with_values != 0, n, begin_bit, end_bit, &a, &b, &c, &d).total;
+}
+
+rs_status rs_sort_host(rs_key_type key_type, const void* h_keys_in, void* h_keys_out,
+                       const uint32_t* h_vals_in, uint32_t* h_vals_out, size_t n, int begin_bit,
+                       int end_bit, void* d_work, size_t work_bytes, void* stream)
+{
+    rs_status st = check_shape(key_type, n, begin_bit, end_bit);
+    if (st != RS_OK) return st;
+    if (n == 0) return RS_OK;
+    const bool vals = h_vals_in || h_vals_out;
+    if (!h_keys_in || !h_keys_out || !d_work || (vals && (!h_vals_in || !h_vals_out)))
+        return RS_ERR_INVALID_ARG;
+    size_t kin, kout, vin, vout;
+    rs::TempLayout t = host_work_layout(key_type, vals, n, begin_bit, end_bit, &kin, &kout, &vin, &vout);
+    if (work_bytes < t.total) return RS_ERR_TEMP_TOO_SMALL;
+    unsigned char* w = static_cast<unsigned char*>(d_work);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t kb = n * key_bytes(key_type);
+    if (cudaMemcpyAsync(w + kin, h_keys_in, kb, cudaMemcpyHostToDevice, s) != cudaSuccess) return RS_ERR_CUDA;
+    if (vals && cudaMemcpyAsync(w + vin, h_vals_in, n * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return RS_ERR_CUDA;
+    rs_sort_desc d{};
+    d.key_type = key_type;
+    d.keys_in = w + kin;
+    d.keys_out = w + kout;
+    d.vals_in = vals ? reinterpret_cast<const uint32_t*>(w + vin) : nullptr;
+    d.vals_out = vals ? reinterpret_cast<uint32_t*>(w + vout) : nullptr;
+    d.n = n;
+    d.begin_bit = begin_bit;
+    d.end_bit = end_bit;
+    d.temp = w;
+    d.temp_bytes = rs::temp_layout(key_bytes(key_type), vals, n, begin_bit, end_bit).total;
+    d.stream = stream;
+    st = rs_sort(&d);
+    if (st != RS_OK) return st;
+    if (cudaMemcpyAsync(h_keys_out, w + kout, kb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return RS_ERR_CUDA;
+    if (vals && cudaMemcpyAsync(h_vals_out, w + vout, n * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return RS_ERR_CUDA;
+    return RS_OK;
+}
+
+}  // extern "C"

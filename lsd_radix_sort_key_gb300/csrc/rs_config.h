@@ -1,0 +1,83 @@
+// rs_config.h -- compile-time shapes shared by the host planner and the kernels.
+//
+// Everything here is plain constexpr arithmetic so that rs_temp_bytes() can
+// size the scratch buffer on a machine without a GPU, and the kernels agree
+// with it by construction.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+namespace rs {
+
+// Largest number of digit passes any request can need (64-bit keys, 4-bit digits).
+constexpr int kMaxPasses = 16;
+
+// The "meta" block at the start of temp: the device error word, one tile
+// ticket per pass (chained scan) and one 256-bin global histogram per pass.
+constexpr int kErrWord = 0;
+constexpr int kTicketBase = 16;
+constexpr int kGhistBase = 64;
+constexpr int kMetaWords = kGhistBase + kMaxPasses * 256;
+
+// Reduce-then-scan: at most this many CTAs, each owning a contiguous chunk.
+constexpr int kRtsMaxCtas = 4096;
+
+// Keys per tile for each (key bytes, has values) combination.  Tiles are
+// THREADS x ITEMS keys with 256 threads; ITEMS is chosen so that keys, ranks
+// and values stay in registers at four resident CTAs per SM.
+constexpr int kTileThreads = 256;
+constexpr int tile_items(int key_bytes, bool vals)
+{
+    return key_bytes == 4 ? (vals ? 12 : 15) : (vals ? 9 : 12);
+}
+constexpr int tile_keys(int key_bytes, bool vals) { return kTileThreads * tile_items(key_bytes, vals); }
+
+constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+constexpr int passes_for(int begin_bit, int end_bit, int radix_bits)
+{
+    return end_bit > begin_bit ? (end_bit - begin_bit + radix_bits - 1) / radix_bits : 0;
+}
+
+// Byte offsets of the regions of temp.  Every region starts on a 256-byte
+// boundary; the meta block (and so the device error word) is always first.
+struct TempLayout {
+    size_t meta;       // kMetaWords uint32
+    size_t alt_keys;   // n keys: the ping-pong partner of keys_out
+    size_t alt_vals;   // n values (pairs only)
+    size_t big;        // chained-scan tile status, or reduce-then-scan block counts
+    size_t big_bytes;
+    size_t total;
+};
+
+constexpr size_t status_bytes(size_t n, int key_bytes, bool vals, int begin_bit, int end_bit,
+                              int radix_bits)
+{
+    size_t tiles = (n + tile_keys(key_bytes, vals) - 1) / tile_keys(key_bytes, vals);
+    return (size_t)passes_for(begin_bit, end_bit, radix_bits) * tiles * ((size_t)1 << radix_bits) * 4;
+}
+
+constexpr TempLayout temp_layout(int key_bytes, bool vals, size_t n, int begin_bit, int end_bit)
+{
+    TempLayout t{};
+    size_t off = 0;
+    t.meta = off;
+    off += align_up(kMetaWords * 4, 256);
+    t.alt_keys = off;
+    off += align_up(n * (size_t)key_bytes, 256);
+    t.alt_vals = off;
+    off += vals ? align_up(n * 4, 256) : 0;
+    t.big = off;
+    size_t s8 = status_bytes(n, key_bytes, vals, begin_bit, end_bit, 8);
+    size_t s4 = status_bytes(n, key_bytes, vals, begin_bit, end_bit, 4);
+    size_t rts = (size_t)256 * kRtsMaxCtas * 4;
+    size_t big = s8 > s4 ? s8 : s4;
+    big = big > rts ? big : rts;
+    t.big_bytes = align_up(big, 256);
+    off += t.big_bytes;
+    t.total = off;
+    return t;
+}
+
+}  // namespace rs

@@ -1,0 +1,51 @@
+"""Helpers for the GPU tests: run the CUDA sort through the C ABI on numpy
+inputs and return numpy outputs."""
+import numpy as np
+
+import lsd_radix_sort_key_gb300 as rs
+
+NP_KEY = {"u32": np.uint32, "i32": np.uint32, "f32": np.uint32, "u64": np.uint64}
+
+
+def to_dev(a, dev):
+    import torch
+    if a is None:
+        return None
+    view = a.view(np.int64) if a.dtype.itemsize == 8 else a.view(np.int32)
+    return torch.from_numpy(np.ascontiguousarray(view)).to(dev)
+
+
+def gpu_sort(kt, keys, vals=None, begin_bit=0, end_bit=None, algo="auto", radix_bits=0,
+             dev="cuda:0", offset=0, in_place=False, check_status=True):
+    """Sort on the GPU via rs_sort; `offset` elements of padding before the
+    input exercise unaligned pointers.  Returns (keys, vals) as numpy."""
+    import torch
+    end_bit = rs.KEY_BITS[kt] if end_bit is None else end_bit
+    n = len(keys)
+    kb = rs.KEY_BYTES[kt]
+    pad_k = np.zeros(offset, dtype=keys.dtype)
+    kin_full = to_dev(np.concatenate([pad_k, keys]) if offset else keys, dev)
+    kin = kin_full[offset:]
+    vin = None
+    if vals is not None:
+        vin_full = to_dev(np.concatenate([np.zeros(offset, np.uint32), vals]) if offset else vals, dev)
+        vin = vin_full[offset:]
+    if in_place:
+        kout, vout = kin, vin
+    else:
+        kout = torch.empty_like(kin) if n else kin
+        vout = None if vin is None else (torch.empty_like(vin) if n else vin)
+    tb = rs.rs_temp_bytes(kt, vals is not None, n, begin_bit, end_bit)
+    temp = torch.empty(max(tb, 256), dtype=torch.uint8, device=dev)
+    d = rs.make_desc(kt, kin if n else None, kout if n else None, vin if n else None,
+                     vout if n else None, n, begin_bit, end_bit, temp, temp.numel(),
+                     None, algo, radix_bits)
+    st = rs.rs_sort(d)
+    assert st == 0, rs.STATUS.get(st, st)
+    torch.cuda.synchronize()
+    if check_status and n:
+        assert rs.rs_device_status(temp) == 0
+    ko = kout.cpu().numpy().view(NP_KEY[kt]) if n else np.empty(0, NP_KEY[kt])
+    vo = None if vals is None else (vout.cpu().numpy().view(np.uint32) if n else np.empty(0, np.uint32))
+    assert kb == ko.dtype.itemsize
+    return ko, vo

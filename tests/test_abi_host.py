@@ -1,0 +1,138 @@
+"""The C-ABI library on the CPU: it loads, exports every declared symbol, and
+rejects bad arguments before touching the GPU (no CUDA call is reached)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import lsd_radix_sort_key_gb300 as rs
+from lsd_radix_sort_key_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return rs.lib()
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"\b(rs_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "rs_sort_keys_u32" in names and "rs_temp_bytes" in names
+    for name in names:
+        assert hasattr(lib, name), name
+        assert name in rs.SIGNATURES, f"binding lacks a signature for {name}"
+
+
+def test_temp_bytes_layout(lib):
+    n = 1 << 20
+    t = rs.rs_temp_bytes("u32", False, n, 0, 32)
+    assert t >= 4 * n  # at least the ping-pong buffer
+    assert rs.rs_temp_bytes("u32", True, n, 0, 32) >= t + 4 * n
+    assert rs.rs_temp_bytes("u64", True, n, 0, 64) > rs.rs_temp_bytes("u32", True, n, 0, 32)
+    assert rs.rs_temp_bytes("u32", False, 0, 0, 32) == 0
+    bad = ctypes.c_size_t(-1).value
+    assert rs.rs_temp_bytes("u32", False, 10, 0, 33) == bad
+    assert rs.rs_temp_bytes("u32", False, 10, 5, 4) == bad
+    assert rs.rs_temp_bytes("u64", False, 10, 0, 65) == bad
+    assert rs.rs_temp_bytes("u32", False, 1 << 33, 0, 32) == bad
+
+
+def test_kernel_counts(lib):
+    def count(kt, n, b, e, algo, rb=0, vals=False):
+        v = 0x3 << 40 if vals else None
+        vo = 0x4 << 40 if vals else None
+        return rs.rs_sort_kernel_count(rs.make_desc(kt, None, None, v, vo, n, b, e, None, 0, 0,
+                                                    algo, rb))
+    assert count("u32", 1 << 20, 0, 32, "onesweep") == 1 + 4
+    assert count("u32", 1 << 20, 0, 30, "onesweep") == 1 + 4
+    assert count("u32", 1 << 20, 0, 32, "onesweep", 4) == 1 + 8
+    assert count("u64", 1 << 20, 0, 64, "onesweep", vals=True) == 1 + 8
+    assert count("u32", 1 << 20, 0, 32, "reduce_scan") == 3 * 4
+    assert count("u32", 1 << 20, 7, 7, "onesweep") == 0
+    assert count("u32", 0, 0, 32, "onesweep") == 0
+    # AUTO picks the chained scan below 2^30 keys
+    assert count("u32", 1 << 20, 0, 32, "auto") == 5
+    assert count("u32", 1 << 30, 0, 32, "auto") == 12
+
+
+FAKE = 1 << 40  # 256-byte aligned addresses that are never dereferenced
+
+
+def desc(**kw):
+    n = kw.pop("n", 1000)
+    base = dict(key_type="u32", keys_in=FAKE, keys_out=2 * FAKE, vals_in=None, vals_out=None,
+                n=n, begin_bit=0, end_bit=32, temp=3 * FAKE,
+                temp_bytes=rs.rs_temp_bytes("u32", True, n, 0, 32), stream=0)
+    base.update(kw)
+    return rs.make_desc(base["key_type"], base["keys_in"], base["keys_out"], base["vals_in"],
+                        base["vals_out"], base["n"], base["begin_bit"], base["end_bit"],
+                        base["temp"], base["temp_bytes"], base["stream"],
+                        kw.get("algo", "auto"), kw.get("radix_bits", 0), 0, kw.get("stall_tile", 0))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(keys_in=None), 1),
+    (dict(keys_out=None), 1),
+    (dict(temp=None), 1),
+    (dict(begin_bit=-1), 1),
+    (dict(end_bit=33), 1),
+    (dict(begin_bit=9, end_bit=8), 1),
+    (dict(key_type="u64", end_bit=65), 1),
+    (dict(radix_bits=5), 1),
+    (dict(vals_in=4 * FAKE), 1),                      # values in without values out
+    (dict(keys_in=FAKE + 2), 1),                      # misaligned for 4-byte keys
+    (dict(temp=3 * FAKE + 16), 1),                    # temp not 256-byte aligned
+    (dict(temp_bytes=100), 2),
+    (dict(keys_out=FAKE + 4 * 500), 3),               # partial overlap
+    (dict(temp=FAKE + 256), 3),                       # temp overlaps the input
+    (dict(n=1 << 31, algo="onesweep"), 7),            # chained scan limited to n < 2^30
+])
+def test_argument_errors(lib, kw, code):
+    d = desc(**kw)
+    assert rs.rs_sort(d) == code
+
+
+def test_n_zero_is_a_no_op(lib):
+    # n == 0 needs no buffers and launches nothing
+    assert rs.rs_sort(desc(n=0, keys_in=None, keys_out=None, temp=None, temp_bytes=0)) == 0
+    assert rs.rs_sort_keys_u32(None, None, 0, 0, 32, None, 0, 0) == 0
+
+
+def test_typed_entry_points_validate(lib):
+    assert rs.rs_sort_keys_u32(FAKE, 2 * FAKE, 100, 0, 40, 3 * FAKE, 1 << 30, 0) == 1
+    assert rs.rs_sort_pairs_f32(FAKE, 2 * FAKE, None, 4 * FAKE, 100, 0, 32, 3 * FAKE, 1 << 30, 0) == 1
+    assert rs.rs_sort_keys_u64(FAKE, 2 * FAKE, 100, 0, 64, 3 * FAKE, 10, 0) == 2
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert rs.rs_status_string(code)
+    assert rs.rs_status_string(99) == "unknown status"
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch):
+    monkeypatch.setattr(rs, "_lib", None)
+    monkeypatch.setattr(rs, "LIB_PATH", "/nonexistent/librs.so")
+    with pytest.raises(RuntimeError, match="missing"):
+        rs.lib()
+
+
+def test_package_does_not_import_oracle():
+    import subprocess
+    import sys
+    code = ("import sys; import lsd_radix_sort_key_gb300 as rs; "
+            "assert 'oracle' not in sys.modules, 'product imported the oracle'")
+    subprocess.check_call([sys.executable, "-c", code], cwd=ROOT)

@@ -1,0 +1,246 @@
+"""Bit-exact parity of the CUDA sort with the CPU oracle (needs a GPU).
+
+Sizes span one tile, several tiles and a ragged tail for every key type, with
+and without values, under both schedules and both digit widths; the edge
+cases cover n = 0..2, empty and partial bit ranges, in-place sorts, unaligned
+pointers, tie-heavy and low-entropy keys, float specials, the CUDA-graph, the
+profiled and the host-buffer entry points, and the look-back timeout path.
+"""
+import numpy as np
+import pytest
+
+import lsd_radix_sort_key_gb300 as rs
+import oracle
+import synth
+from gpu_util import gpu_sort, to_dev
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    rs.build()
+    rs.lib()
+
+
+def gen_keys(kt, n, seed):
+    if kt == "u64":
+        return synth.u64_uniform(n, seed)
+    if kt == "f32":
+        return synth.f32_edge(n, seed)
+    return synth.u32_uniform(n, seed)
+
+
+def check(kt, keys, vals, b, e, **kw):
+    got_k, got_v = gpu_sort(kt, keys, vals, b, e, **kw)
+    ref_k, ref_v = oracle.sort(kt, keys, vals, b, e)
+    assert np.array_equal(got_k, ref_k), f"keys differ ({kt}, n={len(keys)}, [{b},{e}), {kw})"
+    if vals is not None:
+        assert np.array_equal(got_v, ref_v), f"values differ ({kt}, n={len(keys)}, [{b},{e}), {kw})"
+
+
+SIZES = [1, 2, 31, 3839, 3840, 3841, 50_000, (1 << 17) + 123]
+
+
+@pytest.mark.parametrize("algo", ["onesweep", "reduce_scan"])
+@pytest.mark.parametrize("radix_bits", [8, 4])
+@pytest.mark.parametrize("kt", ["u32", "i32", "f32", "u64"])
+@pytest.mark.parametrize("with_vals", [False, True])
+def test_full_range(algo, radix_bits, kt, with_vals):
+    for i, n in enumerate(SIZES):
+        keys = gen_keys(kt, n, 1000 + i)
+        vals = synth.iota_u32(n) if with_vals else None
+        check(kt, keys, vals, 0, rs.KEY_BITS[kt], algo=algo, radix_bits=radix_bits)
+
+
+@pytest.mark.parametrize("algo", ["onesweep", "reduce_scan"])
+@pytest.mark.parametrize("kt", ["u32", "i32", "f32", "u64"])
+def test_partial_bit_ranges(algo, kt):
+    rng = np.random.default_rng(77)
+    bits = rs.KEY_BITS[kt]
+    n = 70_001
+    keys = gen_keys(kt, n, 5)
+    vals = synth.iota_u32(n)
+    ranges = [(0, 1), (bits - 1, bits), (3, 3 + 8), (5, 5 + 13), (0, bits - 2)]
+    ranges += [tuple(sorted(int(x) for x in rng.integers(0, bits + 1, size=2))) for _ in range(4)]
+    for b, e in ranges:
+        check(kt, keys, vals, b, e, algo=algo)
+
+
+@pytest.mark.parametrize("kt", ["u32", "u64"])
+def test_empty_bit_range_is_a_copy(kt):
+    keys = gen_keys(kt, 10_000, 8)
+    vals = synth.iota_u32(10_000)
+    got_k, got_v = gpu_sort(kt, keys, vals, 7, 7)
+    assert np.array_equal(got_k, keys) and np.array_equal(got_v, vals)
+
+
+def test_tiny_and_empty():
+    for n in (0, 1, 2):
+        keys = synth.u32_uniform(n, 3)
+        check("u32", keys, synth.iota_u32(n), 0, 32)
+
+
+@pytest.mark.parametrize("algo", ["onesweep", "reduce_scan"])
+@pytest.mark.parametrize("end_bit", [32, 24])  # even and odd pass counts
+def test_in_place(algo, end_bit):
+    n = 100_003
+    keys = synth.u32_uniform(n, 9)
+    vals = synth.iota_u32(n)
+    got_k, got_v = gpu_sort("u32", keys, vals, 0, end_bit, algo=algo, in_place=True)
+    ref_k, ref_v = oracle.sort("u32", keys, vals, 0, end_bit)
+    assert np.array_equal(got_k, ref_k) and np.array_equal(got_v, ref_v)
+
+
+@pytest.mark.parametrize("offset", [1, 2, 3])
+def test_unaligned_pointers(offset):
+    n = 40_000
+    for kt in ("u32", "f32"):
+        keys = gen_keys(kt, n, 10 + offset)
+        got_k, _ = gpu_sort(kt, keys, None, 0, 32, offset=offset)
+        assert np.array_equal(got_k, oracle.sort(kt, keys)[0])
+    keys = synth.u64_uniform(n, 20 + offset)
+    got_k, got_v = gpu_sort("u64", keys, synth.iota_u32(n), 0, 64, offset=offset)
+    ref = oracle.sort("u64", keys, synth.iota_u32(n))
+    assert np.array_equal(got_k, ref[0]) and np.array_equal(got_v, ref[1])
+
+
+@pytest.mark.parametrize("algo", ["onesweep", "reduce_scan"])
+def test_ties_and_low_entropy(algo):
+    n = 200_000
+    cases = [synth.u32_bits(n, 1, 3),         # 8 distinct keys: stability everywhere
+             synth.u32_and4(n, 2),            # digit 0 holds ~60% of keys in every pass
+             np.full(n, 0xDEADBEEF, np.uint32),
+             np.zeros(n, np.uint32),
+             np.arange(n, dtype=np.uint32)[::-1].copy(),
+             np.arange(n, dtype=np.uint32)]
+    for keys in cases:
+        check("u32", keys, synth.iota_u32(n), 0, 32, algo=algo)
+
+
+def test_float_specials_and_signed_zero():
+    n = 300_000
+    keys = synth.f32_normal_specials(n, 0x5EED0002)
+    vals = synth.iota_u32(n)
+    check("f32", keys, vals, 0, 32)
+    got_k, got_v = gpu_sort("f32", keys, vals)
+    f = got_k.view(np.float32)
+    specials = ~np.isfinite(f)
+    k = int(specials.sum())
+    assert specials[n - k:].all()                      # NaN / +-Inf last ...
+    assert np.all(np.diff(got_v[n - k:].astype(np.int64)) > 0)  # ... in input order
+    zeros = np.nonzero(f == 0)[0]
+    neg = got_k[zeros] == 0x80000000
+    assert neg[: int(neg.sum())].all()                 # -0.0 before +0.0
+
+
+def test_many_tiles_onesweep_lookback():
+    # > 256 tiles per pass, uneven tail: exercises long look-back chains
+    n = (1 << 22) + 12345
+    keys = synth.u32_uniform(n, 31)
+    check("u32", keys, None, 0, 32, algo="onesweep")
+    check("u32", keys, synth.iota_u32(n), 0, 32, algo="reduce_scan")
+
+
+def test_typed_c_entry_points():
+    dev = "cuda:0"
+    n = 123_457
+    for kt in ("u32", "i32", "f32", "u64"):
+        keys = gen_keys(kt, n, 40)
+        vals = synth.iota_u32(n)
+        kin, vin = to_dev(keys, dev), to_dev(vals, dev)
+        kout, vout = torch.empty_like(kin), torch.empty_like(vin)
+        tb = rs.rs_temp_bytes(kt, True, n, 0, rs.KEY_BITS[kt])
+        temp = torch.empty(tb, dtype=torch.uint8, device=dev)
+        fn = getattr(rs, f"rs_sort_pairs_{kt}")
+        assert fn(kin, kout, vin, vout, n, 0, rs.KEY_BITS[kt], temp, tb) == 0
+        kout2 = torch.empty_like(kin)
+        fk = getattr(rs, f"rs_sort_keys_{kt}")
+        assert fk(kin, kout2, n, 0, rs.KEY_BITS[kt], temp, tb) == 0
+        torch.cuda.synchronize()
+        ref_k, ref_v = oracle.sort(kt, keys, vals)
+        assert np.array_equal(kout.cpu().numpy().view(ref_k.dtype), ref_k)
+        assert np.array_equal(vout.cpu().numpy().view(np.uint32), ref_v)
+        assert np.array_equal(kout2.cpu().numpy().view(ref_k.dtype), ref_k)
+
+
+def test_graph_replay():
+    dev = "cuda:0"
+    n = 1 << 16
+    keys = synth.u32_uniform(n, 0x5EED0001)
+    kin = to_dev(keys, dev)
+    kout = torch.empty_like(kin)
+    tb = rs.rs_temp_bytes("u32", False, n, 0, 32)
+    temp = torch.empty(tb, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream()
+    d = rs.make_desc("u32", kin, kout, None, None, n, 0, 32, temp, tb, s)
+    g = rs.Graph(d)
+    ref = oracle.sort("u32", keys)[0]
+    for _ in range(3):
+        kout.zero_()
+        torch.cuda.synchronize()
+        g.launch(s)
+        s.synchronize()
+        assert np.array_equal(kout.cpu().numpy().view(np.uint32), ref)
+    assert rs.rs_device_status(temp, s) == 0
+    g.close()
+
+
+def test_profiled_entry_point():
+    dev = "cuda:0"
+    n = 1 << 20
+    keys = synth.u32_uniform(n, 50)
+    kin = to_dev(keys, dev)
+    kout = torch.empty_like(kin)
+    tb = rs.rs_temp_bytes("u32", False, n, 0, 32)
+    temp = torch.empty(tb, dtype=torch.uint8, device=dev)
+    d = rs.make_desc("u32", kin, kout, None, None, n, 0, 32, temp, tb, None, "onesweep")
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
+    st, kinds = rs.rs_sort_profiled(d, events)
+    assert st == 0
+    assert [rs.KERNEL_KINDS[k] for k in kinds] == ["histogram"] + ["onesweep_pass"] * 4
+    torch.cuda.synchronize()
+    times = [events[i].elapsed_time(events[i + 1]) for i in range(len(kinds))]
+    assert all(t > 0 for t in times)
+    assert np.array_equal(kout.cpu().numpy().view(np.uint32), oracle.sort("u32", keys)[0])
+
+
+def test_host_buffer_entry_point():
+    n = 200_001
+    keys = synth.u64_uniform(n, 60)
+    vals = synth.iota_u32(n)
+    hk = torch.from_numpy(keys.view(np.int64)).pin_memory()
+    hv = torch.from_numpy(vals.view(np.int32)).pin_memory()
+    hko = torch.empty_like(hk).pin_memory()
+    hvo = torch.empty_like(hv).pin_memory()
+    wb = rs.rs_host_work_bytes("u64", True, n, 0, 64)
+    work = torch.empty(wb, dtype=torch.uint8, device="cuda:0")
+    assert rs.rs_sort_host("u64", hk, hko, hv, hvo, n, 0, 64, work, wb) == 0
+    torch.cuda.synchronize()
+    ref_k, ref_v = oracle.sort("u64", keys, vals)
+    assert np.array_equal(hko.numpy().view(np.uint64), ref_k)
+    assert np.array_equal(hvo.numpy().view(np.uint32), ref_v)
+
+
+def test_lookback_timeout_is_reported_and_recoverable():
+    """Tile 3 never publishes: the waits behind it run out after a short bound,
+    the sort reports RS_ERR_DEVICE_TIMEOUT, and the next sort is correct."""
+    dev = "cuda:0"
+    n = 64 * 3840
+    keys = synth.u32_uniform(n, 70)
+    kin = to_dev(keys, dev)
+    kout = torch.empty_like(kin)
+    tb = rs.rs_temp_bytes("u32", False, n, 0, 32)
+    temp = torch.empty(tb, dtype=torch.uint8, device=dev)
+    d = rs.make_desc("u32", kin, kout, None, None, n, 0, 32, temp, tb, None, "onesweep",
+                     0, 2000, 4)
+    assert rs.rs_sort(d) == 0
+    assert rs.rs_device_status(temp) == 5  # RS_ERR_DEVICE_TIMEOUT
+    d2 = rs.make_desc("u32", kin, kout, None, None, n, 0, 32, temp, tb, None, "onesweep")
+    assert rs.rs_sort(d2) == 0
+    assert rs.rs_device_status(temp) == 0
+    assert np.array_equal(kout.cpu().numpy().view(np.uint32), oracle.sort("u32", keys)[0])
