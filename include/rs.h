@@ -200,6 +200,33 @@ rs_status rs_sort_host(rs_key_type key_type, const void* h_keys_in, void* h_keys
                        const uint32_t* h_vals_in, uint32_t* h_vals_out, size_t n, int begin_bit,
                        int end_bit, void* d_work, size_t work_bytes, void* stream);
 
+/*
+ * Sort without any allocation.  The pages have no counterpart to this entry
+ * point; it exists for callers that cannot allocate device memory where they
+ * sort: code running while a stream capture in global mode is active (where
+ * cudaMalloc is not permitted), plugins whose host application owns the
+ * device memory pool, and latency-critical loops where cudaMalloc/cudaFree
+ * would synchronise the device.
+ *
+ * Same operation and arguments as rs_sort_keys_u32, but the scratch is a
+ * fixed array of RS_NOALLOC_SCRATCH_BYTES (about 21 MiB) of device memory
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits.  n must be at most RS_NOALLOC_MAX_N (2^22 keys), else
+ * RS_ERR_INVALID_ARG is returned and nothing is enqueued.  No cudaMalloc,
+ * cudaFree or allocating library routine is called.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  Every call shares the one array per device, so calls that overlap
+ * on the GPU (on different streams, or from different threads) race; each
+ * call clears what must start at zero.  The device error word lives in that
+ * array, so rs_device_status cannot be used with this entry point.
+ */
+#define RS_NOALLOC_MAX_N 4194304
+#define RS_NOALLOC_SCRATCH_BYTES 22020096
+rs_status rs_sort_keys_u32_noalloc(const uint32_t* keys_in, uint32_t* keys_out, size_t n,
+                                   int begin_bit, int end_bit, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -66,6 +66,8 @@ SIGNATURES = {
     "rs_host_work_bytes": (_sz, [_i, _i, _sz, _i, _i]),
     "rs_sort_host": (_i, [_i, _vp, _vp, _vp, _vp, _sz, _i, _i, _vp, _sz, _vp]),
 }
+SIGNATURES["rs_sort_keys_u32_noalloc"] = (_i, [_vp, _vp, _sz, _i, _i, _vp])
+NOALLOC_MAX_N = 1 << 22
 for _t in ("u32", "i32", "f32", "u64"):
     SIGNATURES[f"rs_sort_keys_{_t}"] = _KEYS_SIG
     SIGNATURES[f"rs_sort_pairs_{_t}"] = _PAIRS_SIG
@@ -148,6 +150,13 @@ rs_sort_keys_u32, rs_sort_pairs_u32 = _typed("u32")
 rs_sort_keys_i32, rs_sort_pairs_i32 = _typed("i32")
 rs_sort_keys_f32, rs_sort_pairs_f32 = _typed("f32")
 rs_sort_keys_u64, rs_sort_pairs_u64 = _typed("u64")
+
+
+def rs_sort_keys_u32_noalloc(keys_in, keys_out, n, begin_bit, end_bit, stream=None):
+    """uint32 keys-only sort whose scratch is a fixed device array inside the
+    library (no allocation anywhere; n <= NOALLOC_MAX_N)."""
+    return lib().rs_sort_keys_u32_noalloc(_addr(keys_in), _addr(keys_out), n, begin_bit, end_bit,
+                                          _stream(stream))
 
 
 def make_desc(key_type, keys_in, keys_out, vals_in, vals_out, n, begin_bit, end_bit, temp,
