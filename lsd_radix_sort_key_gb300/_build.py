@@ -42,12 +42,17 @@ def _stale() -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, extra_flags=(), verbose: bool = False) -> str:
-    """Build librs.so if any source is newer than it; returns its path."""
-    if not force and not _stale():
+def build(force: bool = False, extra_flags=(), verbose: bool = False, libdir: str | None = None) -> str:
+    """Build librs.so if any source is newer than it; returns its path.
+
+    extra_flags / libdir build a variant (e.g. -D switches) into another folder.
+    """
+    out_dir = libdir or LIBDIR
+    out_lib = os.path.join(out_dir, "librs.so")
+    if not force and libdir is None and not _stale():
         return LIB
-    os.makedirs(LIBDIR, exist_ok=True)
-    objdir = os.path.join(LIBDIR, "obj")
+    os.makedirs(out_dir, exist_ok=True)
+    objdir = os.path.join(out_dir, "obj")
     os.makedirs(objdir, exist_ok=True)
     common = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "-I", INCLUDE, "-I", CSRC, *extra_flags]
@@ -64,13 +69,13 @@ def build(force: bool = False, extra_flags=(), verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + f".{os.getpid()}.tmp"
+    tmp = out_lib + f".{os.getpid()}.tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out_lib)
+    return out_lib
 
 
 if __name__ == "__main__":

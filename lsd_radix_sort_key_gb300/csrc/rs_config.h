@@ -26,10 +26,16 @@ constexpr int kRtsMaxCtas = 4096;
 // Keys per tile for each (key bytes, has values) combination.  Tiles are
 // THREADS x ITEMS keys with 256 threads; ITEMS is chosen so that keys, ranks
 // and values stay in registers at four resident CTAs per SM.
-constexpr int kTileThreads = 256;
+#ifndef RS_TILE_THREADS
+#define RS_TILE_THREADS 256
+#endif
+#ifndef RS_ITEMS_U32_KEYS
+#define RS_ITEMS_U32_KEYS 15
+#endif
+constexpr int kTileThreads = RS_TILE_THREADS;
 constexpr int tile_items(int key_bytes, bool vals)
 {
-    return key_bytes == 4 ? (vals ? 12 : 15) : (vals ? 9 : 12);
+    return key_bytes == 4 ? (vals ? 12 : RS_ITEMS_U32_KEYS) : (vals ? 9 : 12);
 }
 constexpr int tile_keys(int key_bytes, bool vals) { return kTileThreads * tile_items(key_bytes, vals); }
 

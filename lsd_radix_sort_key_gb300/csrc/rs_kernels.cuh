@@ -39,8 +39,11 @@
 #include "rs.h"
 #include "rs_config.h"
 
+// RS_CHECKED 1 also records (in the device error word) any shuffle position
+// that had to be clamped; the clamp itself and the scatter bounds check are
+// always on.
 #ifndef RS_CHECKED
-#define RS_CHECKED 1
+#define RS_CHECKED 0
 #endif
 
 namespace rs {
@@ -190,46 +193,85 @@ struct TileSmem {
 
 // --------------------------------------------------------------- tile pieces
 
+// Compile-time choices measured against each other (defaults = the faster):
+//   RS_MATCH_BITS   how many high bits of a digit are compared with
+//                   __match_any_sync; the remaining low bits are compared with
+//                   one __ballot_sync each.  (match cost grows with the number
+//                   of distinct values in a warp, ballot cost with the bits.)
+//   RS_LOOKBACK_BATCH  predecessor statuses read at once while walking back.
+//   RS_LOOKBACK_MODE   1: poll the nearest predecessor alone (with a growing
+//                   __nanosleep) and batch only while walking; 0: batch every
+//                   round.
+//   RS_TILE_MIN_THREADS_PER_SM  resident threads per SM the tile kernels are
+//                   compiled for (caps their registers: 1024 -> 64 each).
+#ifndef RS_MATCH_BITS
+#define RS_MATCH_BITS 4
+#endif
+#ifndef RS_LOOKBACK_BATCH
+#define RS_LOOKBACK_BATCH 4
+#endif
+#ifndef RS_LOOKBACK_MODE
+#define RS_LOOKBACK_MODE 1
+#endif
+#ifndef RS_TILE_MIN_THREADS_PER_SM
+#define RS_TILE_MIN_THREADS_PER_SM 1024
+#endif
+
 // Load ITEMS keys per thread in warp-striped order: lane l of warp w holds
 // positions seg + k*32 + l, so every load instruction of a warp covers 32
 // consecutive keys and the processing order (k, lane) is the input order.
-template <typename T, int ITEMS>
+template <bool FULL, typename T, int ITEMS>
 __device__ __forceinline__ void load_striped(const T* __restrict__ src, uint32_t seg, uint32_t n,
-                                             bool full, int lane, T (&v)[ITEMS])
+                                             int lane, T (&v)[ITEMS])
 {
-    if (full) {
 #pragma unroll
-        for (int k = 0; k < ITEMS; ++k) v[k] = src[seg + k * 32 + lane];
-    } else {
-#pragma unroll
-        for (int k = 0; k < ITEMS; ++k) {
-            uint32_t i = seg + k * 32 + lane;
-            v[k] = i < n ? src[i] : T(0);
-        }
+    for (int k = 0; k < ITEMS; ++k) {
+        const uint32_t i = seg + k * 32 + lane;
+        if (FULL) v[k] = src[i];
+        else v[k] = i < n ? src[i] : T(0);
     }
 }
 
-// Stable rank of each key among equal digits within its warp's segment.
-// __match_any_sync gives the lanes holding the same digit in this step; the
-// key's rank is the warp's running count for that digit plus the number of
-// such lanes below it; the highest of those lanes then advances the count.
-// packed[k] = rank | digit << 16 (digit BINS marks a lane past the end).
-template <int KT, int BINS, int ITEMS>
-__device__ __forceinline__ void rank_in_warp(const typename KeyOps<KT>::T (&key)[ITEMS], uint32_t seg,
-                                             uint32_t n, bool full, uint32_t shift, uint32_t mask,
-                                             uint32_t* wh, int lane, uint32_t (&packed)[ITEMS])
+// Mask of the lanes of this warp whose value equals this lane's (the low
+// BITS bits of v are compared; higher bits must be zero).  The top
+// RS_MATCH_BITS of the digit (and any bit above it) go through
+// __match_any_sync, the rest through one __ballot_sync per bit.
+template <int BITS, int RB>
+__device__ __forceinline__ uint32_t warp_peers(uint32_t v)
 {
+    constexpr int BALLOT_BITS = (RB - RS_MATCH_BITS) < 0 ? 0 : (RB - RS_MATCH_BITS);
+    uint32_t peers = (BITS > BALLOT_BITS) ? __match_any_sync(0xFFFFFFFFu, v >> BALLOT_BITS) : 0xFFFFFFFFu;
+#pragma unroll
+    for (int b = 0; b < (BITS < BALLOT_BITS ? BITS : BALLOT_BITS); ++b) {
+        const uint32_t bit = (v >> b) & 1u;
+        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, bit);
+        peers &= bit ? bal : ~bal;
+    }
+    return peers;
+}
+
+// Stable rank of each key among equal digits within its warp's segment.
+// For each step k the lanes holding the same digit (peers) are found; a key's
+// rank is the warp's running count for its digit plus the number of peers
+// below it, and all peers then store the same advanced count (no branch).
+// packed[k] = rank | digit << 16; on a partial tile, lanes past the end get
+// digit BINS, which has its own dummy counter.
+template <bool FULL, int KT, int RB, int ITEMS>
+__device__ __forceinline__ void rank_in_warp(const typename KeyOps<KT>::T (&key)[ITEMS], uint32_t seg,
+                                             uint32_t n, uint32_t shift, uint32_t mask, uint32_t* wh,
+                                             int lane, uint32_t (&packed)[ITEMS])
+{
+    constexpr uint32_t BINS = 1u << RB;
     const uint32_t lt = lanemask_lt();
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
         uint32_t d = digit_of<KT>(key[k], shift, mask);
-        if (!full && seg + k * 32 + lane >= n) d = BINS;
-        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, d);
-        const uint32_t r = wh[d] + __popc(peers & lt);
+        if (!FULL) d = (seg + k * 32 + lane < n) ? d : BINS;
+        const uint32_t peers = warp_peers<FULL ? RB : RB + 1, RB>(d);
+        const uint32_t prior = wh[d];
+        wh[d] = prior + __popc(peers);
+        packed[k] = (prior + __popc(peers & lt)) | (d << 16);
         __syncwarp();
-        if ((peers >> lane) == 1u) wh[d] = r + 1;
-        __syncwarp();
-        packed[k] = r | (d << 16);
     }
 }
 
@@ -238,7 +280,7 @@ __device__ __forceinline__ void rank_in_warp(const typename KeyOps<KT>::T (&key)
 // shared memory.  Returns, for thread d < BINS, the tile's count of digit d in
 // *cnt and its tile-local start in *start.  `publish(d, cnt)` runs for every
 // digit as soon as the count is known (the chained scan publishes it there).
-template <int KT, int RB, int THREADS, int ITEMS, bool VALS, typename Publish>
+template <bool FULL, int KT, int RB, int THREADS, int ITEMS, bool VALS, typename Publish>
 __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsigned char* smem,
                                                       uint32_t tile, uint32_t* cnt_out,
                                                       uint32_t* start_out, Publish publish)
@@ -249,54 +291,61 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
     T* skeys = reinterpret_cast<T*>(smem + S::keys_off);
     uint32_t* svals = reinterpret_cast<uint32_t*>(smem + S::vals_off);
     uint32_t* whist = reinterpret_cast<uint32_t*>(smem + S::wh_off);
-    uint32_t* sbase = reinterpret_cast<uint32_t*>(smem + S::base_off);
     uint32_t* sscan = reinterpret_cast<uint32_t*>(smem + S::scan_off);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t tile_base = tile * (uint32_t)TILE;
-    const bool full = tile_base + (uint32_t)TILE <= p.n;
     const uint32_t seg = tile_base + (uint32_t)warp * (32u * ITEMS);
 
     for (int i = tid; i < WARPS * WH; i += THREADS) whist[i] = 0;
 
     T key[ITEMS];
-    load_striped<T, ITEMS>(static_cast<const T*>(p.keys_in), seg, p.n, full, lane, key);
+    load_striped<FULL, T, ITEMS>(static_cast<const T*>(p.keys_in), seg, p.n, lane, key);
     uint32_t val[VALS ? ITEMS : 1];
-    if constexpr (VALS) load_striped<uint32_t, ITEMS>(p.vals_in, seg, p.n, full, lane, val);
+    if constexpr (VALS) load_striped<FULL, uint32_t, ITEMS>(p.vals_in, seg, p.n, lane, val);
     __syncthreads();  // counters zeroed
 
     uint32_t packed[ITEMS];
-    rank_in_warp<KT, BINS, ITEMS>(key, seg, p.n, full, p.shift, p.mask, whist + warp * WH, lane, packed);
+    rank_in_warp<FULL, KT, RB, ITEMS>(key, seg, p.n, p.shift, p.mask, whist + warp * WH, lane, packed);
     __syncthreads();
 
-    // Per digit: turn the warps' counts into each warp's exclusive offset.
+    // Per digit: the warps' counts, the tile count, and after the scan each
+    // warp's start for the digit inside the tile.
+    uint32_t c[WARPS];
     uint32_t cnt = 0;
     if (tid < BINS) {
 #pragma unroll
         for (int w = 0; w < WARPS; ++w) {
-            uint32_t c = whist[w * WH + tid];
-            whist[w * WH + tid] = cnt;
-            cnt += c;
+            c[w] = whist[w * WH + tid];
+            cnt += c[w];
         }
         publish(tid, cnt);
     }
     const uint32_t start = bins_exclusive_scan<BINS>(tid < BINS ? cnt : 0u, sscan, nullptr);
     if (tid < BINS) {
+        uint32_t run = start;
 #pragma unroll
-        for (int w = 0; w < WARPS; ++w) whist[w * WH + tid] += start;
+        for (int w = 0; w < WARPS; ++w) {
+            whist[w * WH + tid] = run;
+            run += c[w];
+        }
     }
     __syncthreads();
 
-    // Shuffle: each digit becomes one contiguous run of the tile.
+    // Shuffle: each digit becomes one contiguous run of the tile.  pos < TILE
+    // holds by construction; a violation is recorded and clamped, never written
+    // out of bounds.
     uint32_t bad = 0;
+    const uint32_t* wbase = whist + warp * WH;
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
         const uint32_t d = packed[k] >> 16;
-        if (full || d < (uint32_t)BINS) {
-            const uint32_t pos = whist[warp * WH + d] + (packed[k] & 0xFFFFu);
+        uint32_t pos = wbase[d] + (packed[k] & 0xFFFFu);
 #if RS_CHECKED
-            if (pos >= (uint32_t)TILE) { bad = 1; continue; }
+        bad |= pos >= (uint32_t)TILE;
 #endif
+        pos = min(pos, (uint32_t)TILE - 1u);
+        if (FULL || d < (uint32_t)BINS) {
             skeys[pos] = key[k];
             if constexpr (VALS) svals[pos] = val[k];
         }
@@ -304,14 +353,14 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
     if (bad) record_error(p.err, RS_ERR_CHECK_FAILED);
     *cnt_out = cnt;
     *start_out = start;
-    (void)sbase;
 }
 
 // Scatter the shuffled tile: slot s holds a key of digit d, whose global
 // position is sbase[d] + s (sbase = global offset of the digit's run minus
 // its tile-local start).  Consecutive slots mostly share a digit, so each
-// warp store covers few, contiguous segments.
-template <int KT, int RB, int THREADS, int ITEMS, bool VALS>
+// warp store covers few, contiguous segments.  Positions are bounds-checked
+// (a failure is recorded and the store skipped).
+template <bool FULL, int KT, int RB, int THREADS, int ITEMS, bool VALS>
 __device__ __forceinline__ void tile_scatter(const PassParams& p, unsigned char* smem, uint32_t tile)
 {
     using T = typename KeyOps<KT>::T;
@@ -322,89 +371,145 @@ __device__ __forceinline__ void tile_scatter(const PassParams& p, unsigned char*
     const uint32_t* sbase = reinterpret_cast<const uint32_t*>(smem + S::base_off);
     T* out = static_cast<T*>(p.keys_out);
     const uint32_t tile_base = tile * (uint32_t)TILE;
-    const uint32_t valid = p.n - tile_base < (uint32_t)TILE ? p.n - tile_base : (uint32_t)TILE;
+    const uint32_t valid = FULL ? (uint32_t)TILE : p.n - tile_base;
     uint32_t bad = 0;
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
         const uint32_t s = (uint32_t)(k * THREADS) + threadIdx.x;
-        if (s < valid) {
+        if (FULL || s < valid) {
             const T kk = skeys[s];
             const uint32_t idx = sbase[digit_of<KT>(kk, p.shift, p.mask)] + s;
-            if (idx < p.n) {
+            const bool ok = idx < p.n;
+            bad |= !ok;
+            if (ok) {
                 out[idx] = kk;
                 if constexpr (VALS) p.vals_out[idx] = svals[s];
-            } else {
-                bad = 1;
             }
         }
     }
     if (bad) record_error(p.err, RS_ERR_CHECK_FAILED);
 }
 
+// Decoupled look-back for digit d of `tile` (one thread per digit): sum the
+// predecessors' published counts, newest first, until one that already holds
+// an inclusive sum.  RS_LOOKBACK_BATCH statuses are read per round trip; an
+// unpublished status stops the round and is polled again, at most spin_limit
+// times in a row, after which the timeout is recorded and the sum so far
+// returned.
+__device__ __forceinline__ uint32_t lookback(const PassParams& p, uint32_t tile, uint32_t d,
+                                             uint32_t bins)
+{
+    constexpr int B = RS_LOOKBACK_BATCH;
+    uint32_t excl = 0;
+    int32_t t = (int32_t)tile - 1;
+    uint32_t spins = 0;
+#if RS_LOOKBACK_MODE == 1
+    uint32_t sleep_ns = 32;
+#endif
+    while (true) {
+#if RS_LOOKBACK_MODE == 1
+        // Poll the nearest unread status alone until it is published.
+        const uint32_t s0 = ld_relaxed_gpu(p.status + (size_t)t * bins + d);
+        if ((s0 & ~kValMask) == 0u) {
+            if (++spins >= p.spin_limit) break;
+            __nanosleep(sleep_ns);
+            sleep_ns = min(sleep_ns * 2, 1024u);
+            continue;
+        }
+        spins = 0;
+        excl += s0 & kValMask;
+        if ((s0 & ~kValMask) == kFlagInc) return excl;
+        --t;
+        if (t < 0) break;
+#endif
+        // Walk: read B statuses at once, newest first.
+        uint32_t s[B];
+#pragma unroll
+        for (int j = 0; j < B; ++j)
+            s[j] = (t - j >= 0) ? ld_relaxed_gpu(p.status + (size_t)(t - j) * bins + d) : 0u;
+        int consumed = 0;
+        bool stop = false, inclusive = false;
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+            if (!stop) {
+                const uint32_t f = s[j] & ~kValMask;
+                if (f == 0u) {
+                    stop = true;
+                } else {
+                    excl += s[j] & kValMask;
+                    ++consumed;
+                    if (f == kFlagInc) stop = inclusive = true;
+                }
+            }
+        }
+        if (inclusive) return excl;
+        t -= consumed;
+        if (t < 0) break;  // ran past tile 0, which always publishes an inclusive sum
+#if RS_LOOKBACK_MODE != 1
+        if (consumed == 0 && ++spins >= p.spin_limit) break;
+        if (consumed) spins = 0;
+#endif
+    }
+    record_error(p.err, RS_ERR_DEVICE_TIMEOUT);
+    __threadfence();
+    return excl;
+}
+
 // ------------------------------------------------------------------ kernels
 
-// Chained-scan pass: one CTA per tile, tiles numbered by an atomic ticket so
-// that every tile a CTA waits on belongs to a CTA that started earlier.
-template <int KT, int RB, int THREADS, int ITEMS, bool VALS>
-__global__ void __launch_bounds__(THREADS) k_onesweep(PassParams p)
+template <bool FULL, int KT, int RB, int THREADS, int ITEMS, bool VALS>
+__device__ __forceinline__ void onesweep_tile(const PassParams& p, unsigned char* smem, uint32_t tile)
 {
     using T = typename KeyOps<KT>::T;
     using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
     constexpr int BINS = S::BINS;
-    extern __shared__ __align__(16) unsigned char smem[];
     uint32_t* sbase = reinterpret_cast<uint32_t*>(smem + S::base_off);
     uint32_t* sscan = reinterpret_cast<uint32_t*>(smem + S::scan_off);
-    uint32_t* smisc = reinterpret_cast<uint32_t*>(smem + S::misc_off);
     const int tid = threadIdx.x;
-
-    if (tid == 0) smisc[0] = atomicAdd(p.ticket, 1u);
-    __syncthreads();
-    const uint32_t tile = smisc[0];
     const bool stalled = (int32_t)tile + 1 == p.stall_tile;
     uint32_t* my_status = p.status + (size_t)tile * BINS;
 
     // Tile 0 needs the pass's global digit starts: an exclusive scan of the
-    // histogram.  Its published value is then already inclusive.
+    // histogram.  Its published value is then already inclusive and absolute.
     uint32_t gexcl = 0;
     if (tile == 0) gexcl = bins_exclusive_scan<BINS>(tid < BINS ? p.ghist[tid] : 0u, sscan, nullptr);
 
     uint32_t cnt, start;
-    tile_rank_and_shuffle<KT, RB, THREADS, ITEMS, VALS>(
+    tile_rank_and_shuffle<FULL, KT, RB, THREADS, ITEMS, VALS>(
         p, smem, tile, &cnt, &start, [&](int d, uint32_t c) {
             if (stalled) return;
             if (tile == 0) st_relaxed_gpu(my_status + d, kFlagInc | ((gexcl + c) & kValMask));
             else st_relaxed_gpu(my_status + d, kFlagAgg | (c & kValMask));
         });
 
-    // Decoupled look-back, one thread per digit: walk back over predecessor
-    // tiles adding their counts until one that already holds an inclusive sum.
     if (tid < BINS) {
         uint32_t excl = gexcl;
         if (tile > 0) {
-            int32_t t = (int32_t)tile - 1;
-            uint32_t spins = 0;
-            bool timed_out = false;
-            while (t >= 0) {
-                const uint32_t s = ld_relaxed_gpu(p.status + (size_t)t * BINS + tid);
-                const uint32_t f = s & ~kValMask;
-                if (f == 0u) {
-                    if (++spins >= p.spin_limit) { timed_out = true; break; }
-                    continue;
-                }
-                excl += s & kValMask;
-                if (f == kFlagInc) break;
-                --t;
-            }
-            if (timed_out || t < 0) {
-                record_error(p.err, RS_ERR_DEVICE_TIMEOUT);
-                __threadfence();
-            }
+            excl = lookback(p, tile, tid, BINS);
             if (!stalled) st_relaxed_gpu(my_status + tid, kFlagInc | ((excl + cnt) & kValMask));
         }
         sbase[tid] = excl - start;
     }
     __syncthreads();
-    tile_scatter<KT, RB, THREADS, ITEMS, VALS>(p, smem, tile);
+    tile_scatter<FULL, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile);
+}
+
+// Chained-scan pass: one CTA per tile, tiles numbered by an atomic ticket so
+// that every tile a CTA waits on belongs to a CTA that started earlier.
+template <int KT, int RB, int THREADS, int ITEMS, bool VALS>
+__global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS) k_onesweep(PassParams p)
+{
+    using T = typename KeyOps<KT>::T;
+    using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
+    extern __shared__ __align__(16) unsigned char smem[];
+    uint32_t* smisc = reinterpret_cast<uint32_t*>(smem + S::misc_off);
+    if (threadIdx.x == 0) smisc[0] = atomicAdd(p.ticket, 1u);
+    __syncthreads();
+    const uint32_t tile = smisc[0];
+    if ((tile + 1) * (uint32_t)S::TILE <= p.n)
+        onesweep_tile<true, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile);
+    else
+        onesweep_tile<false, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile);
 }
 
 // Reduce-then-scan, step 1: digit histogram of each CTA's chunk, written
@@ -440,61 +545,71 @@ __global__ void __launch_bounds__(THREADS) k_upsweep(PassParams p)
     for (int d = tid; d < BINS; d += THREADS) p.counts[(size_t)d * p.G + g] = hist[d];
 }
 
-// Reduce-then-scan, step 2: exclusive scan, in place, of the m digit-major
-// counts, by one CTA: per-thread segment sums, a block scan of the sums, then
-// each thread rewrites its segment.
+// Reduce-then-scan, step 2: exclusive scan of the digit-major counts.  CTA d
+// scans row d (its G per-CTA counts) in place and writes the row total; the
+// downsweep adds the exclusive scan of the row totals (the digit starts).
 template <int THREADS>
-__global__ void __launch_bounds__(THREADS) k_spine_scan(uint32_t* counts, uint32_t m)
+__global__ void __launch_bounds__(THREADS) k_spine_scan(uint32_t* counts, uint32_t G, uint32_t* row_total)
 {
-    __shared__ uint32_t part[THREADS];
+    __shared__ uint32_t sscan[32];
     const int tid = threadIdx.x;
-    const uint32_t per = (m + THREADS - 1) / THREADS;
-    const uint32_t lo = min(m, tid * per), hi = min(m, lo + per);
+    uint32_t* row = counts + (size_t)blockIdx.x * G;
+    const uint32_t per = (G + THREADS - 1) / THREADS;
+    const uint32_t lo = min(G, tid * per), hi = min(G, lo + per);
     uint32_t sum = 0;
-    for (uint32_t i = lo; i < hi; ++i) sum += counts[i];
-    part[tid] = sum;
-    __syncthreads();
-    // Hillis-Steele scan of THREADS partial sums in shared memory (inclusive).
-    for (int o = 1; o < THREADS; o <<= 1) {
-        uint32_t v = tid >= o ? part[tid - o] : 0u;
-        __syncthreads();
-        part[tid] += v;
-        __syncthreads();
-    }
-    uint32_t run = part[tid] - sum;
+    for (uint32_t i = lo; i < hi; ++i) sum += row[i];
+    uint32_t total;
+    uint32_t run = bins_exclusive_scan<THREADS>(sum, sscan, &total);
     for (uint32_t i = lo; i < hi; ++i) {
-        uint32_t c = counts[i];
-        counts[i] = run;
+        const uint32_t c = row[i];
+        row[i] = run;
         run += c;
     }
+    if (tid == 0) row_total[blockIdx.x] = total;
 }
 
 // Reduce-then-scan, step 3: each CTA walks its chunk tile by tile, keeping a
 // running global offset per digit.
+template <bool FULL, int KT, int RB, int THREADS, int ITEMS, bool VALS>
+__device__ __forceinline__ void downsweep_tile(const PassParams& p, unsigned char* smem, uint32_t tile,
+                                               uint32_t& running)
+{
+    using T = typename KeyOps<KT>::T;
+    using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
+    constexpr int BINS = S::BINS;
+    uint32_t* sbase = reinterpret_cast<uint32_t*>(smem + S::base_off);
+    const int tid = threadIdx.x;
+    uint32_t cnt, start;
+    tile_rank_and_shuffle<FULL, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, &cnt, &start,
+                                                               [](int, uint32_t) {});
+    if (tid < BINS) {
+        sbase[tid] = running - start;
+        running += cnt;
+    }
+    __syncthreads();
+    tile_scatter<FULL, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile);
+    __syncthreads();  // the next tile reuses shared memory
+}
+
 template <int KT, int RB, int THREADS, int ITEMS, bool VALS>
-__global__ void __launch_bounds__(THREADS) k_downsweep(PassParams p)
+__global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS) k_downsweep(PassParams p)
 {
     using T = typename KeyOps<KT>::T;
     using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
     constexpr int BINS = S::BINS;
     extern __shared__ __align__(16) unsigned char smem[];
-    uint32_t* sbase = reinterpret_cast<uint32_t*>(smem + S::base_off);
+    uint32_t* sscan = reinterpret_cast<uint32_t*>(smem + S::scan_off);
     const int tid = threadIdx.x;
     const uint32_t g = blockIdx.x;
-    uint32_t running = tid < BINS ? p.counts[(size_t)tid * p.G + g] : 0u;
+    const uint32_t dstart = bins_exclusive_scan<BINS>(tid < BINS ? p.ghist[tid] : 0u, sscan, nullptr);
+    uint32_t running = tid < BINS ? dstart + p.counts[(size_t)tid * p.G + g] : 0u;
     const uint32_t t0 = g * p.tiles_per_cta;
     const uint32_t t1 = min(p.num_tiles, t0 + p.tiles_per_cta);
     for (uint32_t tile = t0; tile < t1; ++tile) {
-        uint32_t cnt, start;
-        tile_rank_and_shuffle<KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, &cnt, &start,
-                                                             [](int, uint32_t) {});
-        if (tid < BINS) {
-            sbase[tid] = running - start;
-            running += cnt;
-        }
-        __syncthreads();
-        tile_scatter<KT, RB, THREADS, ITEMS, VALS>(p, smem, tile);
-        __syncthreads();  // the next tile reuses shared memory
+        if ((tile + 1) * (uint32_t)S::TILE <= p.n)
+            downsweep_tile<true, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, running);
+        else
+            downsweep_tile<false, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, running);
     }
 }
 
@@ -513,26 +628,33 @@ struct HistParams {
     int aligned16;          // keys pointer is 16-byte aligned
 };
 
-template <int KT, int RB, int THREADS>
+// Counters are lane-private columns, hist[pass][bin][col] with col = lane %
+// COLS, so the COLS lanes of a warp that share no column hit distinct banks:
+// the shared atomics of one warp instruction do not conflict (the warps of
+// the CTA still share the columns, which the atomics make safe).
+template <int KT, int RB, int THREADS, int COLS>
 __global__ void __launch_bounds__(THREADS) k_histogram(HistParams h)
 {
     using T = typename KeyOps<KT>::T;
     constexpr int BINS = 1 << RB;
     constexpr int VEC = 16 / sizeof(T);
+    constexpr int U = 4;  // vectors in flight per thread
     extern __shared__ __align__(16) unsigned char smem[];
     uint32_t* hist = reinterpret_cast<uint32_t*>(smem);
     const int tid = threadIdx.x;
-    const uint32_t words = h.passes * BINS;
+    const uint32_t col = tid % COLS;
+    const uint32_t words = h.passes * BINS * COLS;
     for (uint32_t i = tid; i < words; i += THREADS) hist[i] = 0;
     __syncthreads();
 
     auto count = [&](T k) {
         const auto o = KeyOps<KT>::ordered(k);
         uint32_t shift = h.begin_bit;
-        for (uint32_t q = 0; q < h.passes; ++q, shift += RB) {
+        uint32_t* row = hist + col;
+        for (uint32_t q = 0; q < h.passes; ++q, shift += RB, row += BINS * COLS) {
             const uint32_t width = min((uint32_t)RB, h.end_bit - shift);
             const uint32_t d = (uint32_t)(o >> shift) & ((1u << width) - 1u);
-            atomicAdd(&hist[q * BINS + d], 1u);
+            atomicAdd(row + d * COLS, 1u);
         }
     };
 
@@ -543,8 +665,21 @@ __global__ void __launch_bounds__(THREADS) k_histogram(HistParams h)
     if (h.aligned16) {
         const size_t nvec = h.n / VEC;
         const uint4* kv = reinterpret_cast<const uint4*>(keys);
-        for (size_t v = gid; v < nvec; v += gthreads) {
-            const uint4 w = kv[v];
+        size_t v = gid;
+        for (; v + (U - 1) * gthreads < nvec; v += U * gthreads) {
+            uint4 w[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) w[u] = __ldcs(kv + v + u * gthreads);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                T k[VEC];
+                memcpy(k, &w[u], 16);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) count(k[j]);
+            }
+        }
+        for (; v < nvec; v += gthreads) {
+            const uint4 w = __ldcs(kv + v);
             T k[VEC];
             memcpy(k, &w, 16);
 #pragma unroll
@@ -554,8 +689,10 @@ __global__ void __launch_bounds__(THREADS) k_histogram(HistParams h)
     }
     for (size_t i = done + gid; i < h.n; i += gthreads) count(keys[i]);
     __syncthreads();
-    for (uint32_t i = tid; i < words; i += THREADS) {
-        const uint32_t c = hist[i];
+    for (uint32_t i = tid; i < h.passes * BINS; i += THREADS) {
+        uint32_t c = 0;
+#pragma unroll 8
+        for (int j = 0; j < COLS; ++j) c += hist[i * COLS + ((j + i) % COLS)];
         if (c) atomicAdd(&h.ghist[i], c);
     }
     for (size_t i = gid; i < h.zero_vec4; i += gthreads) h.zero[i] = make_uint4(0, 0, 0, 0);
@@ -674,7 +811,9 @@ rs_status run_passes(Plan& pl)
     base.stall_tile = pl.stall_tile;
 
     if (pl.algo == RS_ALGO_ONESWEEP) {
-        auto hk = k_histogram<KT, RB, 512>;
+        constexpr int MAXP = (8 * KB + RB - 1) / RB;
+        constexpr int HCOLS = (MAXP * (1 << RB) * 32 * 4 <= 160 * 1024) ? 32 : 16;
+        auto hk = k_histogram<KT, RB, 1024, HCOLS>;
         auto pk = k_onesweep<KT, RB, THREADS, ITEMS, VALS>;
         if (!pl.count_only && !set_smem(pk, S::bytes)) return RS_ERR_CUDA;
         const size_t status_words = (size_t)P * num_tiles * BINS;
@@ -689,9 +828,11 @@ rs_status run_passes(Plan& pl)
         h.zero_vec4 = status_words / 4;
         h.aligned16 = (reinterpret_cast<uintptr_t>(pl.keys_in) % 16) == 0;
         const int sms = pl.count_only ? 1 : device_sm_count();
-        const size_t want = (n + 512 * 16 - 1) / (512 * 16);
-        const int hgrid = (int)std::max<size_t>(1, std::min<size_t>(want, (size_t)sms * 2));
-        if (!pl.count_only) hk<<<hgrid, 512, (size_t)P * BINS * 4, pl.stream>>>(h);
+        const size_t want = (n + 1024 * 16 - 1) / (1024 * 16);
+        const int hgrid = (int)std::max<size_t>(1, std::min<size_t>(want, (size_t)sms));
+        const size_t hsmem = (size_t)P * BINS * HCOLS * 4;
+        if (!pl.count_only && !set_smem(hk, hsmem)) return RS_ERR_CUDA;
+        if (!pl.count_only) hk<<<hgrid, 1024, hsmem, pl.stream>>>(h);
         rs_status st = after_launch(pl, kKindHistogram);
         if (st != RS_OK) return st;
         for (int q = 0; q < P; ++q) {
@@ -742,7 +883,9 @@ rs_status run_passes(Plan& pl)
         if (!pl.count_only) uk<<<G, 512, 0, pl.stream>>>(pp);
         rs_status st = after_launch(pl, kKindUpsweep);
         if (st != RS_OK) return st;
-        if (!pl.count_only) k_spine_scan<1024><<<1, 1024, 0, pl.stream>>>(big, (uint32_t)BINS * G);
+        pp.ghist = meta + kGhistBase + q * BINS;  // row totals of this pass
+        if (!pl.count_only)
+            k_spine_scan<256><<<BINS, 256, 0, pl.stream>>>(big, G, meta + kGhistBase + q * BINS);
         st = after_launch(pl, kKindSpine);
         if (st != RS_OK) return st;
         if (!pl.count_only) dk<<<G, THREADS, S::bytes, pl.stream>>>(pp);
