@@ -323,7 +323,7 @@ def run_ours(args):
                                "avg_ms": round(statistics.mean(v), 4),
                                "share": round(sum(v) / sum(sum(x) for x in per_kind.values()), 4)}
                for k, v in per_kind.items()}
-    resolved = args.algo if args.algo != "auto" else ("onesweep" if n < (1 << 30) else "reduce_scan")
+    resolved = "onesweep" if 2 in per_kind else "reduce_scan"
     scheme_bpk = ((kbytes if resolved == "onesweep" else passes * kbytes)
                   + passes * 2 * (kbytes + vbytes))
     ideal_bpk = passes * 2 * (kbytes + vbytes)

@@ -47,8 +47,8 @@
  *     look-back wait that ran out, an index that failed its bounds check) are
  *     written to an error word inside `temp` and read by rs_device_status().
  *   Sizes.  n may be 0 (nothing is launched).  n must be at most
- *     2^32 - 2^16 (the chained-scan schedule needs n < 2^30 and AUTO falls
- *     back to reduce-then-scan above that).  0 <= begin_bit <= end_bit <= 32 (64 for
+ *     2^32 - 2^16 (the chained-scan schedule needs n < 2^30; AUTO uses
+ *     reduce-then-scan above that).  0 <= begin_bit <= end_bit <= 32 (64 for
  *     uint64); begin_bit == end_bit is a stable copy.
  *   Errors.  Invalid arguments return an error before anything is enqueued;
  *     RS_ERR_CUDA reports a failed launch or copy (cudaGetLastError).
@@ -77,7 +77,8 @@ typedef enum rs_status {
 typedef enum rs_key_type { RS_U32 = 0, RS_I32 = 1, RS_F32 = 2, RS_U64 = 3 } rs_key_type;
 
 typedef enum rs_algo {
-    RS_ALGO_AUTO = 0,        /* chained scan when n < 2^30, else reduce-then-scan   */
+    RS_ALGO_AUTO = 0,        /* reduce-then-scan for 32-bit keys-only n >= 2^25 and
+                                for n >= 2^30; the chained scan otherwise        */
     RS_ALGO_ONESWEEP = 1,    /* one upfront histogram read + one kernel per pass    */
     RS_ALGO_REDUCE_SCAN = 2  /* upsweep + spine scan + downsweep per pass           */
 } rs_algo;

@@ -23,6 +23,7 @@ namespace {
 
 constexpr size_t kMaxN = (size_t)0xFFFF0000u;        // 2^32 - 2^16
 constexpr size_t kOnesweepMaxN = ((size_t)1 << 30) - 1;
+constexpr size_t kAutoReduceScanMinN = (size_t)1 << 25;
 constexpr uint32_t kDefaultSpinLimit = 1u << 20;      // each spin is one L2 round trip (~1 s in all)
 
 int key_bytes(rs_key_type kt) { return kt == RS_U64 ? 8 : 4; }
@@ -67,7 +68,13 @@ rs_status make_plan(const rs_sort_desc* d, rs::Plan* pl)
     pl->radix_bits = d->radix_bits == 0 ? 8 : d->radix_bits;
     pl->passes = rs::passes_for(d->begin_bit, d->end_bit, pl->radix_bits);
     pl->algo = d->algo;
-    if (pl->algo == RS_ALGO_AUTO) pl->algo = n <= kOnesweepMaxN ? RS_ALGO_ONESWEEP : RS_ALGO_REDUCE_SCAN;
+    if (pl->algo == RS_ALGO_AUTO) {
+        // Chosen by measurement on GB300: reduce-then-scan is faster for large
+        // 32-bit keys-only sorts, the chained scan for everything else (and it
+        // needs n < 2^30).
+        const bool rts = n > kOnesweepMaxN || (!vals && kb == 4 && n >= kAutoReduceScanMinN);
+        pl->algo = rts ? RS_ALGO_REDUCE_SCAN : RS_ALGO_ONESWEEP;
+    }
     if (pl->algo == RS_ALGO_ONESWEEP && n > kOnesweepMaxN) return RS_ERR_UNSUPPORTED;
     pl->keys_in = d->keys_in;
     pl->keys_out = d->keys_out;

@@ -23,21 +23,30 @@ constexpr int kMetaWords = kGhistBase + kMaxPasses * 256;
 // Reduce-then-scan: at most this many CTAs, each owning a contiguous chunk.
 constexpr int kRtsMaxCtas = 4096;
 
-// Keys per tile for each (key bytes, has values) combination.  Tiles are
-// THREADS x ITEMS keys with 256 threads; ITEMS is chosen so that keys, ranks
-// and values stay in registers at four resident CTAs per SM.
-#ifndef RS_TILE_THREADS
-#define RS_TILE_THREADS 256
+// Tile shapes.  A tile is THREADS x ITEMS keys; ITEMS is chosen per (key
+// bytes, has values) so that keys, packed ranks and values stay in registers
+// at 1024 resident threads per SM (64 registers each).  The chained-scan pass
+// uses larger tiles than the reduce-then-scan downsweep: fewer tiles mean a
+// shorter look-back and less status traffic.  (Measured on 2^28 uint32 keys.)
+#ifndef RS_RTS_THREADS
+#define RS_RTS_THREADS 256
+#endif
+#ifndef RS_OS_THREADS
+#define RS_OS_THREADS 512
 #endif
 #ifndef RS_ITEMS_U32_KEYS
-#define RS_ITEMS_U32_KEYS 15
+#define RS_ITEMS_U32_KEYS 16
 #endif
-constexpr int kTileThreads = RS_TILE_THREADS;
+enum : int { kAlgoOnesweep = 1, kAlgoReduceScan = 2 };
+constexpr int tile_threads(int algo) { return algo == kAlgoOnesweep ? RS_OS_THREADS : RS_RTS_THREADS; }
 constexpr int tile_items(int key_bytes, bool vals)
 {
     return key_bytes == 4 ? (vals ? 12 : RS_ITEMS_U32_KEYS) : (vals ? 9 : 12);
 }
-constexpr int tile_keys(int key_bytes, bool vals) { return kTileThreads * tile_items(key_bytes, vals); }
+constexpr int tile_keys(int algo, int key_bytes, bool vals)
+{
+    return tile_threads(algo) * tile_items(key_bytes, vals);
+}
 
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -60,7 +69,8 @@ struct TempLayout {
 constexpr size_t status_bytes(size_t n, int key_bytes, bool vals, int begin_bit, int end_bit,
                               int radix_bits)
 {
-    size_t tiles = (n + tile_keys(key_bytes, vals) - 1) / tile_keys(key_bytes, vals);
+    const size_t tk = (size_t)tile_keys(kAlgoOnesweep, key_bytes, vals);
+    size_t tiles = (n + tk - 1) / tk;
     return (size_t)passes_for(begin_bit, end_bit, radix_bits) * tiles * ((size_t)1 << radix_bits) * 4;
 }
 

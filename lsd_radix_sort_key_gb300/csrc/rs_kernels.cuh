@@ -199,22 +199,24 @@ struct TileSmem {
 //                   one __ballot_sync each.  (match cost grows with the number
 //                   of distinct values in a warp, ballot cost with the bits.)
 //   RS_LOOKBACK_BATCH  predecessor statuses read at once while walking back.
-//   RS_LOOKBACK_MODE   1: poll the nearest predecessor alone (with a growing
-//                   __nanosleep) and batch only while walking; 0: batch every
-//                   round.
 //   RS_TILE_MIN_THREADS_PER_SM  resident threads per SM the tile kernels are
 //                   compiled for (caps their registers: 1024 -> 64 each).
 #ifndef RS_MATCH_BITS
-#define RS_MATCH_BITS 4
+#define RS_MATCH_BITS 3
+#endif
+#ifndef RS_BALLOT_XOR
+#define RS_BALLOT_XOR 1
 #endif
 #ifndef RS_LOOKBACK_BATCH
 #define RS_LOOKBACK_BATCH 4
 #endif
-#ifndef RS_LOOKBACK_MODE
-#define RS_LOOKBACK_MODE 1
-#endif
 #ifndef RS_TILE_MIN_THREADS_PER_SM
 #define RS_TILE_MIN_THREADS_PER_SM 1024
+#endif
+//   RS_OS_PERSISTENT   1: chained-scan CTAs loop over tiles and prefetch the
+//                   next one; 0: one tile per CTA.
+#ifndef RS_OS_PERSISTENT
+#define RS_OS_PERSISTENT 0
 #endif
 
 // Load ITEMS keys per thread in warp-striped order: lane l of warp w holds
@@ -232,6 +234,26 @@ __device__ __forceinline__ void load_striped(const T* __restrict__ src, uint32_t
     }
 }
 
+// Keys (and values) of one tile in warp-striped order; a tile that runs past
+// n is guarded lane by lane.
+template <int KT, int THREADS, int ITEMS, bool VALS>
+__device__ __forceinline__ void load_tile(const PassParams& p, uint32_t tile,
+                                          typename KeyOps<KT>::T (&key)[ITEMS],
+                                          uint32_t (&val)[VALS ? ITEMS : 1])
+{
+    using T = typename KeyOps<KT>::T;
+    constexpr uint32_t TILE = THREADS * ITEMS;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t seg = tile * TILE + (uint32_t)warp * (32u * ITEMS);
+    if ((tile + 1) * TILE <= p.n) {
+        load_striped<true, T, ITEMS>(static_cast<const T*>(p.keys_in), seg, p.n, lane, key);
+        if constexpr (VALS) load_striped<true, uint32_t, ITEMS>(p.vals_in, seg, p.n, lane, val);
+    } else {
+        load_striped<false, T, ITEMS>(static_cast<const T*>(p.keys_in), seg, p.n, lane, key);
+        if constexpr (VALS) load_striped<false, uint32_t, ITEMS>(p.vals_in, seg, p.n, lane, val);
+    }
+}
+
 // Mask of the lanes of this warp whose value equals this lane's (the low
 // BITS bits of v are compared; higher bits must be zero).  The top
 // RS_MATCH_BITS of the digit (and any bit above it) go through
@@ -245,7 +267,11 @@ __device__ __forceinline__ uint32_t warp_peers(uint32_t v)
     for (int b = 0; b < (BITS < BALLOT_BITS ? BITS : BALLOT_BITS); ++b) {
         const uint32_t bit = (v >> b) & 1u;
         const uint32_t bal = __ballot_sync(0xFFFFFFFFu, bit);
+#if RS_BALLOT_XOR
+        peers &= bal ^ (bit - 1u);  // bit - 1 is all ones exactly when the bit is clear
+#else
         peers &= bit ? bal : ~bal;
+#endif
     }
     return peers;
 }
@@ -254,36 +280,50 @@ __device__ __forceinline__ uint32_t warp_peers(uint32_t v)
 // For each step k the lanes holding the same digit (peers) are found; a key's
 // rank is the warp's running count for its digit plus the number of peers
 // below it, and all peers then store the same advanced count (no branch).
-// packed[k] = rank | digit << 16; on a partial tile, lanes past the end get
-// digit BINS, which has its own dummy counter.
+// Ranks (< 2^16) are packed two per register: rank[k/2] holds step k in its
+// low half when k is even, in its high half when k is odd.  On a partial
+// tile, lanes past the end get digit BINS, which has its own dummy counter.
+template <bool FULL, int KT, int RB, int ITEMS>
+__device__ __forceinline__ uint32_t step_digit(const typename KeyOps<KT>::T (&key)[ITEMS], int k, uint32_t seg,
+                                               uint32_t n, uint32_t shift, uint32_t mask, int lane)
+{
+    const uint32_t d = digit_of<KT>(key[k], shift, mask);
+    return (FULL || seg + k * 32 + lane < n) ? d : (1u << RB);
+}
+
 template <bool FULL, int KT, int RB, int ITEMS>
 __device__ __forceinline__ void rank_in_warp(const typename KeyOps<KT>::T (&key)[ITEMS], uint32_t seg,
                                              uint32_t n, uint32_t shift, uint32_t mask, uint32_t* wh,
-                                             int lane, uint32_t (&packed)[ITEMS])
+                                             int lane, uint32_t (&rank)[(ITEMS + 1) / 2])
 {
-    constexpr uint32_t BINS = 1u << RB;
     const uint32_t lt = lanemask_lt();
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
-        uint32_t d = digit_of<KT>(key[k], shift, mask);
-        if (!FULL) d = (seg + k * 32 + lane < n) ? d : BINS;
+        const uint32_t d = step_digit<FULL, KT, RB, ITEMS>(key, k, seg, n, shift, mask, lane);
         const uint32_t peers = warp_peers<FULL ? RB : RB + 1, RB>(d);
         const uint32_t prior = wh[d];
         wh[d] = prior + __popc(peers);
-        packed[k] = (prior + __popc(peers & lt)) | (d << 16);
+        const uint32_t r = prior + __popc(peers & lt);
+        if (k & 1) rank[k / 2] |= r << 16;
+        else rank[k / 2] = r;
         __syncwarp();
     }
 }
 
-// Everything of one tile up to the point where its global digit offsets are
-// needed: load, rank, per-digit counts, tile-local digit starts, shuffle into
-// shared memory.  Returns, for thread d < BINS, the tile's count of digit d in
-// *cnt and its tile-local start in *start.  `publish(d, cnt)` runs for every
-// digit as soon as the count is known (the chained scan publishes it there).
+// Everything of one tile, whose keys are in registers, up to the point where
+// its global digit offsets are needed: rank, per-digit counts, tile-local
+// digit starts, shuffle into shared memory.  Returns, for thread d < BINS,
+// the tile's count of digit d in *cnt and its tile-local start in *start.
+// `publish(d, cnt)` runs for every digit as soon as the count is known (the
+// chained scan publishes it there).  The key/value registers are free again
+// on return (the caller prefetches the next tile into them).
 template <bool FULL, int KT, int RB, int THREADS, int ITEMS, bool VALS, typename Publish>
 __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsigned char* smem,
-                                                      uint32_t tile, uint32_t* cnt_out,
-                                                      uint32_t* start_out, Publish publish)
+                                                      uint32_t tile,
+                                                      const typename KeyOps<KT>::T (&key)[ITEMS],
+                                                      const uint32_t (&val)[VALS ? ITEMS : 1],
+                                                      uint32_t* cnt_out, uint32_t* start_out,
+                                                      Publish publish)
 {
     using T = typename KeyOps<KT>::T;
     using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
@@ -298,27 +338,19 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
     const uint32_t seg = tile_base + (uint32_t)warp * (32u * ITEMS);
 
     for (int i = tid; i < WARPS * WH; i += THREADS) whist[i] = 0;
-
-    T key[ITEMS];
-    load_striped<FULL, T, ITEMS>(static_cast<const T*>(p.keys_in), seg, p.n, lane, key);
-    uint32_t val[VALS ? ITEMS : 1];
-    if constexpr (VALS) load_striped<FULL, uint32_t, ITEMS>(p.vals_in, seg, p.n, lane, val);
     __syncthreads();  // counters zeroed
 
-    uint32_t packed[ITEMS];
-    rank_in_warp<FULL, KT, RB, ITEMS>(key, seg, p.n, p.shift, p.mask, whist + warp * WH, lane, packed);
+    uint32_t rank[(ITEMS + 1) / 2];
+    rank_in_warp<FULL, KT, RB, ITEMS>(key, seg, p.n, p.shift, p.mask, whist + warp * WH, lane, rank);
     __syncthreads();
 
-    // Per digit: the warps' counts, the tile count, and after the scan each
-    // warp's start for the digit inside the tile.
-    uint32_t c[WARPS];
+    // Per digit: the tile count, and after the scan each warp's start for the
+    // digit inside the tile (the warps' counts are read twice rather than
+    // held in registers).
     uint32_t cnt = 0;
     if (tid < BINS) {
 #pragma unroll
-        for (int w = 0; w < WARPS; ++w) {
-            c[w] = whist[w * WH + tid];
-            cnt += c[w];
-        }
+        for (int w = 0; w < WARPS; ++w) cnt += whist[w * WH + tid];
         publish(tid, cnt);
     }
     const uint32_t start = bins_exclusive_scan<BINS>(tid < BINS ? cnt : 0u, sscan, nullptr);
@@ -326,21 +358,22 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
         uint32_t run = start;
 #pragma unroll
         for (int w = 0; w < WARPS; ++w) {
+            const uint32_t c = whist[w * WH + tid];
             whist[w * WH + tid] = run;
-            run += c[w];
+            run += c;
         }
     }
     __syncthreads();
 
     // Shuffle: each digit becomes one contiguous run of the tile.  pos < TILE
-    // holds by construction; a violation is recorded and clamped, never written
-    // out of bounds.
+    // holds by construction; the clamp keeps a violation inside the tile.
     uint32_t bad = 0;
     const uint32_t* wbase = whist + warp * WH;
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
-        const uint32_t d = packed[k] >> 16;
-        uint32_t pos = wbase[d] + (packed[k] & 0xFFFFu);
+        const uint32_t d = step_digit<FULL, KT, RB, ITEMS>(key, k, seg, p.n, p.shift, p.mask, lane);
+        const uint32_t r = (k & 1) ? (rank[k / 2] >> 16) : (rank[k / 2] & 0xFFFFu);
+        uint32_t pos = wbase[d] + r;
 #if RS_CHECKED
         bad |= pos >= (uint32_t)TILE;
 #endif
@@ -396,37 +429,32 @@ __device__ __forceinline__ void tile_scatter(const PassParams& p, unsigned char*
 // unpublished status stops the round and is polled again, at most spin_limit
 // times in a row, after which the timeout is recorded and the sum so far
 // returned.
-__device__ __forceinline__ uint32_t lookback(const PassParams& p, uint32_t tile, uint32_t d,
-                                             uint32_t bins)
+// The first RS_LOOKBACK_BATCH statuses are read early (pre[], issued before
+// the tile's shuffle so that their latency overlaps it); the walk then goes
+// on from where they leave off.
+template <int B>
+__device__ __forceinline__ void lookback_preload(const PassParams& p, uint32_t tile, uint32_t d,
+                                                 uint32_t bins, uint32_t (&pre)[B])
 {
-    constexpr int B = RS_LOOKBACK_BATCH;
+    const int32_t t = (int32_t)tile - 1;
+#pragma unroll
+    for (int j = 0; j < B; ++j)
+        pre[j] = (t - j >= 0) ? ld_relaxed_gpu(p.status + (size_t)(t - j) * bins + d) : 0u;
+}
+
+template <int B>
+__device__ __forceinline__ uint32_t lookback(const PassParams& p, uint32_t tile, uint32_t d, uint32_t bins,
+                                             const uint32_t (&pre)[B])
+{
     uint32_t excl = 0;
     int32_t t = (int32_t)tile - 1;
-    uint32_t spins = 0;
-#if RS_LOOKBACK_MODE == 1
-    uint32_t sleep_ns = 32;
-#endif
-    while (true) {
-#if RS_LOOKBACK_MODE == 1
-        // Poll the nearest unread status alone until it is published.
-        const uint32_t s0 = ld_relaxed_gpu(p.status + (size_t)t * bins + d);
-        if ((s0 & ~kValMask) == 0u) {
-            if (++spins >= p.spin_limit) break;
-            __nanosleep(sleep_ns);
-            sleep_ns = min(sleep_ns * 2, 1024u);
-            continue;
-        }
-        spins = 0;
-        excl += s0 & kValMask;
-        if ((s0 & ~kValMask) == kFlagInc) return excl;
-        --t;
-        if (t < 0) break;
-#endif
-        // Walk: read B statuses at once, newest first.
-        uint32_t s[B];
+    uint32_t spins = 0, sleep_ns = 0;
+    uint32_t s[B];
 #pragma unroll
-        for (int j = 0; j < B; ++j)
-            s[j] = (t - j >= 0) ? ld_relaxed_gpu(p.status + (size_t)(t - j) * bins + d) : 0u;
+    for (int j = 0; j < B; ++j) s[j] = pre[j];
+    while (true) {
+        // Consume the newest-first batch up to an unpublished status or an
+        // inclusive one.
         int consumed = 0;
         bool stop = false, inclusive = false;
 #pragma unroll
@@ -445,10 +473,21 @@ __device__ __forceinline__ uint32_t lookback(const PassParams& p, uint32_t tile,
         if (inclusive) return excl;
         t -= consumed;
         if (t < 0) break;  // ran past tile 0, which always publishes an inclusive sum
-#if RS_LOOKBACK_MODE != 1
-        if (consumed == 0 && ++spins >= p.spin_limit) break;
-        if (consumed) spins = 0;
-#endif
+        if (consumed == 0) {
+            // The nearest unread status is not published yet: poll it alone.
+            if (++spins >= p.spin_limit) break;
+            if (sleep_ns) __nanosleep(sleep_ns);
+            sleep_ns = sleep_ns ? min(sleep_ns * 2, 256u) : 16u;
+            s[0] = ld_relaxed_gpu(p.status + (size_t)t * bins + d);
+#pragma unroll
+            for (int j = 1; j < B; ++j) s[j] = 0u;
+            continue;
+        }
+        spins = 0;
+        sleep_ns = 0;
+#pragma unroll
+        for (int j = 0; j < B; ++j)
+            s[j] = (t - j >= 0) ? ld_relaxed_gpu(p.status + (size_t)(t - j) * bins + d) : 0u;
     }
     record_error(p.err, RS_ERR_DEVICE_TIMEOUT);
     __threadfence();
@@ -457,8 +496,13 @@ __device__ __forceinline__ uint32_t lookback(const PassParams& p, uint32_t tile,
 
 // ------------------------------------------------------------------ kernels
 
+// One tile of a chained-scan pass.  `next` is the ticket this CTA already
+// holds for its following tile; that tile's keys are loaded into the freed
+// registers while this tile looks back and scatters.
 template <bool FULL, int KT, int RB, int THREADS, int ITEMS, bool VALS>
-__device__ __forceinline__ void onesweep_tile(const PassParams& p, unsigned char* smem, uint32_t tile)
+__device__ __forceinline__ void onesweep_tile(const PassParams& p, unsigned char* smem, uint32_t tile,
+                                              uint32_t next, typename KeyOps<KT>::T (&key)[ITEMS],
+                                              uint32_t (&val)[VALS ? ITEMS : 1])
 {
     using T = typename KeyOps<KT>::T;
     using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
@@ -475,17 +519,21 @@ __device__ __forceinline__ void onesweep_tile(const PassParams& p, unsigned char
     if (tile == 0) gexcl = bins_exclusive_scan<BINS>(tid < BINS ? p.ghist[tid] : 0u, sscan, nullptr);
 
     uint32_t cnt, start;
+    uint32_t pre[RS_LOOKBACK_BATCH];
     tile_rank_and_shuffle<FULL, KT, RB, THREADS, ITEMS, VALS>(
-        p, smem, tile, &cnt, &start, [&](int d, uint32_t c) {
-            if (stalled) return;
-            if (tile == 0) st_relaxed_gpu(my_status + d, kFlagInc | ((gexcl + c) & kValMask));
-            else st_relaxed_gpu(my_status + d, kFlagAgg | (c & kValMask));
+        p, smem, tile, key, val, &cnt, &start, [&](int d, uint32_t c) {
+            if (!stalled) {
+                if (tile == 0) st_relaxed_gpu(my_status + d, kFlagInc | ((gexcl + c) & kValMask));
+                else st_relaxed_gpu(my_status + d, kFlagAgg | (c & kValMask));
+            }
+            if (tile > 0) lookback_preload<RS_LOOKBACK_BATCH>(p, tile, d, BINS, pre);
         });
+    if (next < p.num_tiles) load_tile<KT, THREADS, ITEMS, VALS>(p, next, key, val);
 
     if (tid < BINS) {
         uint32_t excl = gexcl;
         if (tile > 0) {
-            excl = lookback(p, tile, tid, BINS);
+            excl = lookback<RS_LOOKBACK_BATCH>(p, tile, tid, BINS, pre);
             if (!stalled) st_relaxed_gpu(my_status + tid, kFlagInc | ((excl + cnt) & kValMask));
         }
         sbase[tid] = excl - start;
@@ -494,8 +542,10 @@ __device__ __forceinline__ void onesweep_tile(const PassParams& p, unsigned char
     tile_scatter<FULL, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile);
 }
 
-// Chained-scan pass: one CTA per tile, tiles numbered by an atomic ticket so
-// that every tile a CTA waits on belongs to a CTA that started earlier.
+// Chained-scan pass, persistent: each CTA takes tiles by an atomic ticket
+// until none is left.  Tickets are handed out in order, so every tile a CTA
+// waits on belongs to a CTA that already runs (and that CTA finishes the
+// tile it holds before the one it prefetches).
 template <int KT, int RB, int THREADS, int ITEMS, bool VALS>
 __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS) k_onesweep(PassParams p)
 {
@@ -503,13 +553,30 @@ __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS)
     using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
     extern __shared__ __align__(16) unsigned char smem[];
     uint32_t* smisc = reinterpret_cast<uint32_t*>(smem + S::misc_off);
-    if (threadIdx.x == 0) smisc[0] = atomicAdd(p.ticket, 1u);
+    const int tid = threadIdx.x;
+    if (tid == 0) smisc[0] = atomicAdd(p.ticket, 1u);
     __syncthreads();
-    const uint32_t tile = smisc[0];
-    if ((tile + 1) * (uint32_t)S::TILE <= p.n)
-        onesweep_tile<true, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile);
-    else
-        onesweep_tile<false, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile);
+    uint32_t tile = smisc[0];
+    if (tile >= p.num_tiles) return;
+    T key[ITEMS];
+    uint32_t val[VALS ? ITEMS : 1];
+    load_tile<KT, THREADS, ITEMS, VALS>(p, tile, key, val);
+    while (true) {
+#if RS_OS_PERSISTENT
+        __syncthreads();  // the previous tile's scatter is done with shared memory
+        if (tid == 0) smisc[1] = atomicAdd(p.ticket, 1u);
+        __syncthreads();
+        const uint32_t next = smisc[1];
+#else
+        const uint32_t next = 0xFFFFFFFFu;
+#endif
+        if ((tile + 1) * (uint32_t)S::TILE <= p.n)
+            onesweep_tile<true, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, next, key, val);
+        else
+            onesweep_tile<false, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, next, key, val);
+        if (next >= p.num_tiles) break;
+        tile = next;
+    }
 }
 
 // Reduce-then-scan, step 1: digit histogram of each CTA's chunk, written
@@ -572,7 +639,9 @@ __global__ void __launch_bounds__(THREADS) k_spine_scan(uint32_t* counts, uint32
 // running global offset per digit.
 template <bool FULL, int KT, int RB, int THREADS, int ITEMS, bool VALS>
 __device__ __forceinline__ void downsweep_tile(const PassParams& p, unsigned char* smem, uint32_t tile,
-                                               uint32_t& running)
+                                               uint32_t next, uint32_t& running,
+                                               typename KeyOps<KT>::T (&key)[ITEMS],
+                                               uint32_t (&val)[VALS ? ITEMS : 1])
 {
     using T = typename KeyOps<KT>::T;
     using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
@@ -580,8 +649,9 @@ __device__ __forceinline__ void downsweep_tile(const PassParams& p, unsigned cha
     uint32_t* sbase = reinterpret_cast<uint32_t*>(smem + S::base_off);
     const int tid = threadIdx.x;
     uint32_t cnt, start;
-    tile_rank_and_shuffle<FULL, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, &cnt, &start,
+    tile_rank_and_shuffle<FULL, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, key, val, &cnt, &start,
                                                                [](int, uint32_t) {});
+    if (next != 0xFFFFFFFFu) load_tile<KT, THREADS, ITEMS, VALS>(p, next, key, val);
     if (tid < BINS) {
         sbase[tid] = running - start;
         running += cnt;
@@ -605,11 +675,16 @@ __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS)
     uint32_t running = tid < BINS ? dstart + p.counts[(size_t)tid * p.G + g] : 0u;
     const uint32_t t0 = g * p.tiles_per_cta;
     const uint32_t t1 = min(p.num_tiles, t0 + p.tiles_per_cta);
+    if (t0 >= t1) return;
+    T key[ITEMS];
+    uint32_t val[VALS ? ITEMS : 1];
+    load_tile<KT, THREADS, ITEMS, VALS>(p, t0, key, val);
     for (uint32_t tile = t0; tile < t1; ++tile) {
+        const uint32_t next = tile + 1 < t1 ? tile + 1 : 0xFFFFFFFFu;
         if ((tile + 1) * (uint32_t)S::TILE <= p.n)
-            downsweep_tile<true, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, running);
+            downsweep_tile<true, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, next, running, key, val);
         else
-            downsweep_tile<false, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, running);
+            downsweep_tile<false, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, next, running, key, val);
     }
 }
 
@@ -768,14 +843,9 @@ rs_status run_passes(Plan& pl)
 {
     using T = typename KeyOps<KT>::T;
     constexpr int KB = sizeof(T);
-    constexpr int THREADS = kTileThreads;
     constexpr int ITEMS = tile_items(KB, VALS);
-    constexpr int TILE = THREADS * ITEMS;
     constexpr int BINS = 1 << RB;
-    using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
-
     const uint32_t n = (uint32_t)pl.n;
-    const uint32_t num_tiles = (n + TILE - 1) / TILE;
     uint32_t* meta = reinterpret_cast<uint32_t*>(pl.temp + pl.lay.meta);
     uint32_t* big = reinterpret_cast<uint32_t*>(pl.temp + pl.lay.big);
     T* alt_keys = reinterpret_cast<T*>(pl.temp + pl.lay.alt_keys);
@@ -805,12 +875,16 @@ rs_status run_passes(Plan& pl)
 
     PassParams base{};
     base.n = n;
-    base.num_tiles = num_tiles;
     base.err = meta + kErrWord;
     base.spin_limit = pl.spin_limit;
     base.stall_tile = pl.stall_tile;
 
     if (pl.algo == RS_ALGO_ONESWEEP) {
+        constexpr int THREADS = tile_threads(kAlgoOnesweep);
+        constexpr int TILE = THREADS * ITEMS;
+        using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
+        const uint32_t num_tiles = (n + TILE - 1) / TILE;
+        base.num_tiles = num_tiles;
         constexpr int MAXP = (8 * KB + RB - 1) / RB;
         constexpr int HCOLS = (MAXP * (1 << RB) * 32 * 4 <= 160 * 1024) ? 32 : 16;
         auto hk = k_histogram<KT, RB, 1024, HCOLS>;
@@ -835,6 +909,13 @@ rs_status run_passes(Plan& pl)
         if (!pl.count_only) hk<<<hgrid, 1024, hsmem, pl.stream>>>(h);
         rs_status st = after_launch(pl, kKindHistogram);
         if (st != RS_OK) return st;
+        uint32_t os_grid = num_tiles;
+        if (!pl.count_only) {
+            int occ = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, pk, THREADS, S::bytes) != cudaSuccess || occ < 1)
+                occ = 1;
+            os_grid = RS_OS_PERSISTENT ? (uint32_t)std::min<size_t>((size_t)sms * occ, num_tiles) : num_tiles;
+        }
         for (int q = 0; q < P; ++q) {
             PassParams pp = base;
             pp.keys_in = q == 0 ? (const void*)src_keys0 : (const void*)dst_keys(q - 1);
@@ -847,7 +928,7 @@ rs_status run_passes(Plan& pl)
             pp.status = big + (size_t)q * num_tiles * BINS;
             pp.ghist = meta + kGhistBase + q * BINS;
             pp.ticket = meta + kTicketBase + q;
-            if (!pl.count_only) pk<<<num_tiles, THREADS, S::bytes, pl.stream>>>(pp);
+            if (!pl.count_only) pk<<<os_grid, THREADS, S::bytes, pl.stream>>>(pp);
             st = after_launch(pl, kKindOnesweep);
             if (st != RS_OK) return st;
         }
@@ -855,6 +936,11 @@ rs_status run_passes(Plan& pl)
     }
 
     // Reduce-then-scan.
+    constexpr int THREADS = tile_threads(kAlgoReduceScan);
+    constexpr int TILE = THREADS * ITEMS;
+    using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
+    const uint32_t num_tiles = (n + TILE - 1) / TILE;
+    base.num_tiles = num_tiles;
     auto uk = k_upsweep<KT, RB, 512, TILE>;
     auto dk = k_downsweep<KT, RB, THREADS, ITEMS, VALS>;
     if (!pl.count_only && !set_smem(dk, S::bytes)) return RS_ERR_CUDA;

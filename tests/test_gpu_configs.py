@@ -2,9 +2,9 @@
 
 Every workload runs at its full size in the launch configuration the bench
 times (the default schedule and digit width), and the whole output is
-compared with the oracle's, element by element.  The reduce-then-scan
-schedule is also checked at 2^28 keys, and the size sweep's largest point
-(2^29 uint32 keys) once.
+compared with the oracle's, element by element.  The schedule the default
+does not pick for 2^28 uint32 keys (the chained scan) is also checked at
+that size, and the size sweep's largest point (2^29 uint32 keys) once.
 """
 import numpy as np
 import pytest
@@ -44,8 +44,12 @@ def test_workload_full_size(name):
     run_workload(synth.WORKLOADS[name])
 
 
-def test_reduce_then_scan_full_size():
-    run_workload(synth.WORKLOADS["c4a_u32_2p28"], algo="reduce_scan")
+def test_chained_scan_full_size():
+    run_workload(synth.WORKLOADS["c4a_u32_2p28"], algo="onesweep")
+
+
+def test_reduce_then_scan_pairs_full_size():
+    run_workload(synth.WORKLOADS["c4b_morton_2p28"], algo="reduce_scan")
 
 
 def test_sweep_largest_size():
