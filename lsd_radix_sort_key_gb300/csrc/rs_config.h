@@ -39,9 +39,12 @@ constexpr int kRtsMaxCtas = 4096;
 #endif
 enum : int { kAlgoOnesweep = 1, kAlgoReduceScan = 2 };
 constexpr int tile_threads(int algo) { return algo == kAlgoOnesweep ? RS_OS_THREADS : RS_RTS_THREADS; }
+#ifndef RS_ITEMS_U32_PAIRS
+#define RS_ITEMS_U32_PAIRS 12
+#endif
 constexpr int tile_items(int key_bytes, bool vals)
 {
-    return key_bytes == 4 ? (vals ? 12 : RS_ITEMS_U32_KEYS) : (vals ? 9 : 12);
+    return key_bytes == 4 ? (vals ? RS_ITEMS_U32_PAIRS : RS_ITEMS_U32_KEYS) : (vals ? 9 : 12);
 }
 constexpr int tile_keys(int algo, int key_bytes, bool vals)
 {

@@ -46,6 +46,38 @@
 #define RS_CHECKED 0
 #endif
 
+// Compile-time choices measured against each other (defaults = the faster):
+//   RS_MATCH_BITS   how many high bits of a digit are compared with
+//                   __match_any_sync; the remaining low bits are compared with
+//                   one __ballot_sync each.  (match cost grows with the number
+//                   of distinct values in a warp, ballot cost with the bits.)
+//   RS_LOOKBACK_BATCH  predecessor statuses read at once while walking back.
+//   RS_TILE_MIN_THREADS_PER_SM  resident threads per SM the tile kernels are
+//                   compiled for (caps their registers: 1024 -> 64 each).
+#ifndef RS_MATCH_BITS
+#define RS_MATCH_BITS 3
+#endif
+#ifndef RS_BALLOT_XOR
+#define RS_BALLOT_XOR 1
+#endif
+#ifndef RS_LOOKBACK_BATCH
+#define RS_LOOKBACK_BATCH 4
+#endif
+#ifndef RS_TILE_MIN_THREADS_PER_SM
+#define RS_TILE_MIN_THREADS_PER_SM 1024
+#endif
+//   RS_CHAINS       each warp's segment is split into this many contiguous
+//                   parts with separate digit counters ("virtual warps"),
+//                   ranked interleaved: independent dependency chains.
+#ifndef RS_CHAINS
+#define RS_CHAINS 1
+#endif
+//   RS_OS_PERSISTENT   1: chained-scan CTAs loop over tiles and prefetch the
+//                   next one; 0: one tile per CTA.
+#ifndef RS_OS_PERSISTENT
+#define RS_OS_PERSISTENT 0
+#endif
+
 namespace rs {
 
 enum : int { KU32 = 0, KI32 = 1, KF32 = 2, KU64 = 3 };
@@ -180,44 +212,20 @@ template <typename T, int RB, int THREADS, int ITEMS, bool VALS>
 struct TileSmem {
     static constexpr int BINS = 1 << RB;
     static constexpr int WARPS = THREADS / 32;
+    static constexpr int CHAINS = (ITEMS % RS_CHAINS == 0) ? RS_CHAINS : 1;
+    static constexpr int VWARPS = WARPS * CHAINS;  // counter arrays ("virtual warps")
     static constexpr int TILE = THREADS * ITEMS;
-    static constexpr int WH = BINS + 1;  // per-warp counters + one dummy slot for tail lanes
+    static constexpr int WH = BINS + 1;  // per-array counters + one dummy slot for tail lanes
     static constexpr size_t keys_off = 0;
     static constexpr size_t vals_off = align_up(sizeof(T) * TILE, 16);
     static constexpr size_t wh_off = vals_off + (VALS ? align_up(4 * (size_t)TILE, 16) : 0);
-    static constexpr size_t base_off = wh_off + align_up(4 * (size_t)WARPS * WH, 16);
+    static constexpr size_t base_off = wh_off + align_up(4 * (size_t)VWARPS * WH, 16);
     static constexpr size_t scan_off = base_off + 4 * BINS;
     static constexpr size_t misc_off = scan_off + 4 * 32;
     static constexpr size_t bytes = misc_off + 16;
 };
 
 // --------------------------------------------------------------- tile pieces
-
-// Compile-time choices measured against each other (defaults = the faster):
-//   RS_MATCH_BITS   how many high bits of a digit are compared with
-//                   __match_any_sync; the remaining low bits are compared with
-//                   one __ballot_sync each.  (match cost grows with the number
-//                   of distinct values in a warp, ballot cost with the bits.)
-//   RS_LOOKBACK_BATCH  predecessor statuses read at once while walking back.
-//   RS_TILE_MIN_THREADS_PER_SM  resident threads per SM the tile kernels are
-//                   compiled for (caps their registers: 1024 -> 64 each).
-#ifndef RS_MATCH_BITS
-#define RS_MATCH_BITS 3
-#endif
-#ifndef RS_BALLOT_XOR
-#define RS_BALLOT_XOR 1
-#endif
-#ifndef RS_LOOKBACK_BATCH
-#define RS_LOOKBACK_BATCH 4
-#endif
-#ifndef RS_TILE_MIN_THREADS_PER_SM
-#define RS_TILE_MIN_THREADS_PER_SM 1024
-#endif
-//   RS_OS_PERSISTENT   1: chained-scan CTAs loop over tiles and prefetch the
-//                   next one; 0: one tile per CTA.
-#ifndef RS_OS_PERSISTENT
-#define RS_OS_PERSISTENT 0
-#endif
 
 // Load ITEMS keys per thread in warp-striped order: lane l of warp w holds
 // positions seg + k*32 + l, so every load instruction of a warp covers 32
@@ -291,21 +299,30 @@ __device__ __forceinline__ uint32_t step_digit(const typename KeyOps<KT>::T (&ke
     return (FULL || seg + k * 32 + lane < n) ? d : (1u << RB);
 }
 
-template <bool FULL, int KT, int RB, int ITEMS>
+template <bool FULL, int KT, int RB, int ITEMS, int CHAINS, int WH>
 __device__ __forceinline__ void rank_in_warp(const typename KeyOps<KT>::T (&key)[ITEMS], uint32_t seg,
                                              uint32_t n, uint32_t shift, uint32_t mask, uint32_t* wh,
                                              int lane, uint32_t (&rank)[(ITEMS + 1) / 2])
 {
+    // Part c holds steps [c*L, (c+1)*L) and counts into wh + c*WH; the parts
+    // are visited interleaved (j-th step of every part, then the next j).
+    constexpr int L = ITEMS / CHAINS;
     const uint32_t lt = lanemask_lt();
 #pragma unroll
-    for (int k = 0; k < ITEMS; ++k) {
-        const uint32_t d = step_digit<FULL, KT, RB, ITEMS>(key, k, seg, n, shift, mask, lane);
-        const uint32_t peers = warp_peers<FULL ? RB : RB + 1, RB>(d);
-        const uint32_t prior = wh[d];
-        wh[d] = prior + __popc(peers);
-        const uint32_t r = prior + __popc(peers & lt);
-        if (k & 1) rank[k / 2] |= r << 16;
-        else rank[k / 2] = r;
+    for (int i = 0; i < (ITEMS + 1) / 2; ++i) rank[i] = 0;
+#pragma unroll
+    for (int j = 0; j < L; ++j) {
+#pragma unroll
+        for (int c = 0; c < CHAINS; ++c) {
+            const int k = c * L + j;
+            uint32_t* cnt = wh + c * WH;
+            const uint32_t d = step_digit<FULL, KT, RB, ITEMS>(key, k, seg, n, shift, mask, lane);
+            const uint32_t peers = warp_peers<FULL ? RB : RB + 1, RB>(d);
+            const uint32_t prior = cnt[d];
+            cnt[d] = prior + __popc(peers);
+            const uint32_t r = prior + __popc(peers & lt);
+            rank[k / 2] |= (k & 1) ? (r << 16) : r;
+        }
         __syncwarp();
     }
 }
@@ -327,7 +344,7 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
 {
     using T = typename KeyOps<KT>::T;
     using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
-    constexpr int BINS = S::BINS, WARPS = S::WARPS, TILE = S::TILE, WH = S::WH;
+    constexpr int BINS = S::BINS, TILE = S::TILE, WH = S::WH, CHAINS = S::CHAINS, VWARPS = S::VWARPS;
     T* skeys = reinterpret_cast<T*>(smem + S::keys_off);
     uint32_t* svals = reinterpret_cast<uint32_t*>(smem + S::vals_off);
     uint32_t* whist = reinterpret_cast<uint32_t*>(smem + S::wh_off);
@@ -337,11 +354,12 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
     const uint32_t tile_base = tile * (uint32_t)TILE;
     const uint32_t seg = tile_base + (uint32_t)warp * (32u * ITEMS);
 
-    for (int i = tid; i < WARPS * WH; i += THREADS) whist[i] = 0;
+    for (int i = tid; i < VWARPS * WH; i += THREADS) whist[i] = 0;
     __syncthreads();  // counters zeroed
 
     uint32_t rank[(ITEMS + 1) / 2];
-    rank_in_warp<FULL, KT, RB, ITEMS>(key, seg, p.n, p.shift, p.mask, whist + warp * WH, lane, rank);
+    rank_in_warp<FULL, KT, RB, ITEMS, CHAINS, WH>(key, seg, p.n, p.shift, p.mask,
+                                                  whist + warp * CHAINS * WH, lane, rank);
     __syncthreads();
 
     // Per digit: the tile count, and after the scan each warp's start for the
@@ -350,14 +368,14 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
     uint32_t cnt = 0;
     if (tid < BINS) {
 #pragma unroll
-        for (int w = 0; w < WARPS; ++w) cnt += whist[w * WH + tid];
+        for (int w = 0; w < VWARPS; ++w) cnt += whist[w * WH + tid];
         publish(tid, cnt);
     }
     const uint32_t start = bins_exclusive_scan<BINS>(tid < BINS ? cnt : 0u, sscan, nullptr);
     if (tid < BINS) {
         uint32_t run = start;
 #pragma unroll
-        for (int w = 0; w < WARPS; ++w) {
+        for (int w = 0; w < VWARPS; ++w) {
             const uint32_t c = whist[w * WH + tid];
             whist[w * WH + tid] = run;
             run += c;
@@ -368,12 +386,12 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
     // Shuffle: each digit becomes one contiguous run of the tile.  pos < TILE
     // holds by construction; the clamp keeps a violation inside the tile.
     uint32_t bad = 0;
-    const uint32_t* wbase = whist + warp * WH;
+    const uint32_t* wbase = whist + warp * CHAINS * WH;
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
         const uint32_t d = step_digit<FULL, KT, RB, ITEMS>(key, k, seg, p.n, p.shift, p.mask, lane);
         const uint32_t r = (k & 1) ? (rank[k / 2] >> 16) : (rank[k / 2] & 0xFFFFu);
-        uint32_t pos = wbase[d] + r;
+        uint32_t pos = wbase[(k / (ITEMS / CHAINS)) * WH + d] + r;
 #if RS_CHECKED
         bad |= pos >= (uint32_t)TILE;
 #endif
