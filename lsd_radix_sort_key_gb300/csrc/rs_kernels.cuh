@@ -81,6 +81,9 @@
 namespace rs {
 
 enum : int { KU32 = 0, KI32 = 1, KF32 = 2, KU64 = 3 };
+// The same 32-bit key types, for passes whose digit is one whole byte of the
+// ordered key: the digit is then one byte permute instead of a shift and a mask.
+enum : int { KU32B = 4, KI32B = 5, KF32B = 6 };
 
 // ------------------------------------------------------------------ key maps
 
@@ -117,10 +120,20 @@ template <> struct KeyOps<KU64> {
     static __device__ __forceinline__ uint64_t ordered(uint64_t u) { return u; }
 };
 
+template <> struct KeyOps<KU32B> : KeyOps<KU32> { static constexpr bool kByte = true; };
+template <> struct KeyOps<KI32B> : KeyOps<KI32> { static constexpr bool kByte = true; };
+template <> struct KeyOps<KF32B> : KeyOps<KF32> { static constexpr bool kByte = true; };
+
+template <int KT, typename = void> struct IsByte { static constexpr bool value = false; };
+template <int KT> struct IsByte<KT, decltype((void)KeyOps<KT>::kByte)> { static constexpr bool value = true; };
+
 template <int KT>
 __device__ __forceinline__ uint32_t digit_of(typename KeyOps<KT>::T u, uint32_t shift, uint32_t mask)
 {
-    return (uint32_t)(KeyOps<KT>::ordered(u) >> shift) & mask;
+    if constexpr (IsByte<KT>::value)  // byte (shift / 8) moved to the low byte, zeros above
+        return __byte_perm((uint32_t)KeyOps<KT>::ordered(u), 0u, 0x4440u | (shift >> 3));
+    else
+        return (uint32_t)(KeyOps<KT>::ordered(u) >> shift) & mask;
 }
 
 // ------------------------------------------------------------- small helpers
@@ -580,7 +593,7 @@ __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS)
     uint32_t val[VALS ? ITEMS : 1];
     load_tile<KT, THREADS, ITEMS, VALS>(p, tile, key, val);
     while (true) {
-#if RS_OS_PERSISTENT
+#if RS_OS_PERSISTENT == 1
         __syncthreads();  // the previous tile's scatter is done with shared memory
         if (tid == 0) smisc[1] = atomicAdd(p.ticket, 1u);
         __syncthreads();
@@ -592,8 +605,18 @@ __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS)
             onesweep_tile<true, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, next, key, val);
         else
             onesweep_tile<false, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, next, key, val);
+#if RS_OS_PERSISTENT == 2
+        // take the next ticket only now, so no tile waits on a held ticket
+        __syncthreads();
+        if (tid == 0) smisc[1] = atomicAdd(p.ticket, 1u);
+        __syncthreads();
+        tile = smisc[1];
+        if (tile >= p.num_tiles) break;
+        load_tile<KT, THREADS, ITEMS, VALS>(p, tile, key, val);
+#else
         if (next >= p.num_tiles) break;
         tile = next;
+#endif
     }
 }
 
@@ -856,6 +879,12 @@ inline bool set_smem(K kernel, size_t bytes)
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) == cudaSuccess;
 }
 
+// The byte-digit twin of a 32-bit key type (the type itself otherwise).
+template <int KT> struct ByteTwin { static constexpr int value = KT; };
+template <> struct ByteTwin<KU32> { static constexpr int value = KU32B; };
+template <> struct ByteTwin<KI32> { static constexpr int value = KI32B; };
+template <> struct ByteTwin<KF32> { static constexpr int value = KF32B; };
+
 template <int KT, int RB, bool VALS>
 rs_status run_passes(Plan& pl)
 {
@@ -907,7 +936,8 @@ rs_status run_passes(Plan& pl)
         constexpr int HCOLS = (MAXP * (1 << RB) * 32 * 4 <= 160 * 1024) ? 32 : 16;
         auto hk = k_histogram<KT, RB, 1024, HCOLS>;
         auto pk = k_onesweep<KT, RB, THREADS, ITEMS, VALS>;
-        if (!pl.count_only && !set_smem(pk, S::bytes)) return RS_ERR_CUDA;
+        auto pkb = k_onesweep<ByteTwin<KT>::value, RB, THREADS, ITEMS, VALS>;
+        if (!pl.count_only && (!set_smem(pk, S::bytes) || !set_smem(pkb, S::bytes))) return RS_ERR_CUDA;
         const size_t status_words = (size_t)P * num_tiles * BINS;
         HistParams h{};
         h.keys = pl.keys_in;
@@ -933,6 +963,7 @@ rs_status run_passes(Plan& pl)
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, pk, THREADS, S::bytes) != cudaSuccess || occ < 1)
                 occ = 1;
             os_grid = RS_OS_PERSISTENT ? (uint32_t)std::min<size_t>((size_t)sms * occ, num_tiles) : num_tiles;
+            (void)pkb;
         }
         for (int q = 0; q < P; ++q) {
             PassParams pp = base;
@@ -946,7 +977,8 @@ rs_status run_passes(Plan& pl)
             pp.status = big + (size_t)q * num_tiles * BINS;
             pp.ghist = meta + kGhistBase + q * BINS;
             pp.ticket = meta + kTicketBase + q;
-            if (!pl.count_only) pk<<<os_grid, THREADS, S::bytes, pl.stream>>>(pp);
+            const bool byte_digit = (RB == 8) && (pp.shift % 8 == 0) && (pp.mask == 0xFFu);
+            if (!pl.count_only) (byte_digit ? pkb : pk)<<<os_grid, THREADS, S::bytes, pl.stream>>>(pp);
             st = after_launch(pl, kKindOnesweep);
             if (st != RS_OK) return st;
         }
@@ -961,7 +993,8 @@ rs_status run_passes(Plan& pl)
     base.num_tiles = num_tiles;
     auto uk = k_upsweep<KT, RB, 512, TILE>;
     auto dk = k_downsweep<KT, RB, THREADS, ITEMS, VALS>;
-    if (!pl.count_only && !set_smem(dk, S::bytes)) return RS_ERR_CUDA;
+    auto dkb = k_downsweep<ByteTwin<KT>::value, RB, THREADS, ITEMS, VALS>;
+    if (!pl.count_only && (!set_smem(dk, S::bytes) || !set_smem(dkb, S::bytes))) return RS_ERR_CUDA;
     uint32_t G = 1;
     if (!pl.count_only) {
         int occ = 0;
@@ -992,7 +1025,8 @@ rs_status run_passes(Plan& pl)
             k_spine_scan<256><<<BINS, 256, 0, pl.stream>>>(big, G, meta + kGhistBase + q * BINS);
         st = after_launch(pl, kKindSpine);
         if (st != RS_OK) return st;
-        if (!pl.count_only) dk<<<G, THREADS, S::bytes, pl.stream>>>(pp);
+        const bool byte_digit = (RB == 8) && (pp.shift % 8 == 0) && (pp.mask == 0xFFu);
+        if (!pl.count_only) (byte_digit ? dkb : dk)<<<G, THREADS, S::bytes, pl.stream>>>(pp);
         st = after_launch(pl, kKindDownsweep);
         if (st != RS_OK) return st;
     }
