@@ -629,9 +629,12 @@ __global__ void __launch_bounds__(THREADS) k_upsweep(PassParams p)
 {
     using T = typename KeyOps<KT>::T;
     constexpr int BINS = 1 << RB;
-    __shared__ uint32_t hist[BINS];
+    constexpr int COLS = 32;          // lane-private counter columns: hist[bin][lane]
+    constexpr int VEC = 16 / sizeof(T);
+    __shared__ uint32_t hist[BINS * COLS];
     const int tid = threadIdx.x;
-    for (int i = tid; i < BINS; i += THREADS) hist[i] = 0;
+    const uint32_t col = tid & 31;
+    for (int i = tid; i < BINS * COLS; i += THREADS) hist[i] = 0;
     __syncthreads();
     const uint32_t g = blockIdx.x;
     const uint64_t lo64 = (uint64_t)g * p.tiles_per_cta * TILE;
@@ -639,18 +642,43 @@ __global__ void __launch_bounds__(THREADS) k_upsweep(PassParams p)
     const uint64_t hi64 = lo64 + (uint64_t)p.tiles_per_cta * TILE;
     const uint32_t hi = hi64 < p.n ? (uint32_t)hi64 : p.n;
     const T* src = static_cast<const T*>(p.keys_in);
-    constexpr int U = 4;
-    uint32_t i = lo + tid;
-    for (; i + (U - 1) * THREADS < hi; i += U * THREADS) {
-        T k[U];
+    auto count = [&](T k) { atomicAdd(&hist[digit_of<KT>(k, p.shift, p.mask) * COLS + col], 1u); };
+    // lo is a multiple of TILE, so lo * sizeof(T) is 16-byte aligned whenever the base is.
+    uint32_t i = lo;
+    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+        constexpr int U = 4;
+        const uint32_t nvec = (hi - lo) / VEC;
+        const uint4* sv = reinterpret_cast<const uint4*>(src + lo);
+        uint32_t v = tid;
+        for (; v + (U - 1) * THREADS < nvec; v += U * THREADS) {
+            uint4 w[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) k[u] = src[i + u * THREADS];
+            for (int u = 0; u < U; ++u) w[u] = __ldcs(sv + v + u * THREADS);
 #pragma unroll
-        for (int u = 0; u < U; ++u) atomicAdd(&hist[digit_of<KT>(k[u], p.shift, p.mask)], 1u);
+            for (int u = 0; u < U; ++u) {
+                T k[VEC];
+                memcpy(k, &w[u], 16);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) count(k[j]);
+            }
+        }
+        for (; v < nvec; v += THREADS) {
+            const uint4 w = __ldcs(sv + v);
+            T k[VEC];
+            memcpy(k, &w, 16);
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) count(k[j]);
+        }
+        i = lo + nvec * VEC;
     }
-    for (; i < hi; i += THREADS) atomicAdd(&hist[digit_of<KT>(src[i], p.shift, p.mask)], 1u);
+    for (i += tid; i < hi; i += THREADS) count(src[i]);
     __syncthreads();
-    for (int d = tid; d < BINS; d += THREADS) p.counts[(size_t)d * p.G + g] = hist[d];
+    for (int d = tid; d < BINS; d += THREADS) {
+        uint32_t c = 0;
+#pragma unroll 8
+        for (int j = 0; j < COLS; ++j) c += hist[d * COLS + ((j + d) & (COLS - 1))];
+        p.counts[(size_t)d * p.G + g] = c;
+    }
 }
 
 // Reduce-then-scan, step 2: exclusive scan of the digit-major counts.  CTA d
