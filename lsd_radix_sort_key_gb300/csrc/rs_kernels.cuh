@@ -167,9 +167,10 @@ __device__ __forceinline__ uint32_t lanemask_lt()
 __device__ __forceinline__ void record_error(uint32_t* err, uint32_t code) { atomicOr(err, 1u << code); }
 
 // Exclusive scan of one value per digit over the first BINS threads of the
-// block (others pass 0).  Every thread must call it: it holds two barriers.
-// `scratch` needs 32 words.  *total (if given) receives the sum.
-template <int BINS>
+// block (others pass 0).  Every thread must call it: it holds one barrier, and
+// a second one unless TRAILING_SYNC is false.  `scratch` needs (BINS + 31) / 32
+// words.  *total (if given) receives the sum.
+template <int BINS, bool TRAILING_SYNC = true>
 __device__ __forceinline__ uint32_t bins_exclusive_scan(uint32_t v, uint32_t* scratch, uint32_t* total)
 {
     constexpr int SCAN_WARPS = (BINS + 31) / 32;
@@ -192,7 +193,9 @@ __device__ __forceinline__ uint32_t bins_exclusive_scan(uint32_t v, uint32_t* sc
         tot += s;
     }
     if (total) *total = tot;
-    __syncthreads();
+    // Without the trailing barrier the caller must not reuse `scratch` before
+    // another block-wide barrier.
+    if (TRAILING_SYNC) __syncthreads();
     return (warp < SCAN_WARPS) ? x - v + wp : 0u;
 }
 
@@ -340,6 +343,14 @@ __device__ __forceinline__ void rank_in_warp(const typename KeyOps<KT>::T (&key)
     }
 }
 
+// Zero the tile's digit counters (the caller synchronises before ranking).
+template <typename S>
+__device__ __forceinline__ void zero_counters(unsigned char* smem, int threads)
+{
+    uint32_t* whist = reinterpret_cast<uint32_t*>(smem + S::wh_off);
+    for (int i = threadIdx.x; i < S::VWARPS * S::WH; i += threads) whist[i] = 0;
+}
+
 // Everything of one tile, whose keys are in registers, up to the point where
 // its global digit offsets are needed: rank, per-digit counts, tile-local
 // digit starts, shuffle into shared memory.  Returns, for thread d < BINS,
@@ -367,9 +378,7 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
     const uint32_t tile_base = tile * (uint32_t)TILE;
     const uint32_t seg = tile_base + (uint32_t)warp * (32u * ITEMS);
 
-    for (int i = tid; i < VWARPS * WH; i += THREADS) whist[i] = 0;
-    __syncthreads();  // counters zeroed
-
+    // (the caller has zeroed the counters and synchronised)
     uint32_t rank[(ITEMS + 1) / 2];
     rank_in_warp<FULL, KT, RB, ITEMS, CHAINS, WH>(key, seg, p.n, p.shift, p.mask,
                                                   whist + warp * CHAINS * WH, lane, rank);
@@ -384,7 +393,7 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
         for (int w = 0; w < VWARPS; ++w) cnt += whist[w * WH + tid];
         publish(tid, cnt);
     }
-    const uint32_t start = bins_exclusive_scan<BINS>(tid < BINS ? cnt : 0u, sscan, nullptr);
+    const uint32_t start = bins_exclusive_scan<BINS, false>(tid < BINS ? cnt : 0u, sscan + 16, nullptr);
     if (tid < BINS) {
         uint32_t run = start;
 #pragma unroll
@@ -586,6 +595,7 @@ __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS)
     uint32_t* smisc = reinterpret_cast<uint32_t*>(smem + S::misc_off);
     const int tid = threadIdx.x;
     if (tid == 0) smisc[0] = atomicAdd(p.ticket, 1u);
+    zero_counters<S>(smem, THREADS);
     __syncthreads();
     uint32_t tile = smisc[0];
     if (tile >= p.num_tiles) return;
@@ -596,6 +606,7 @@ __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS)
 #if RS_OS_PERSISTENT == 1
         __syncthreads();  // the previous tile's scatter is done with shared memory
         if (tid == 0) smisc[1] = atomicAdd(p.ticket, 1u);
+        zero_counters<S>(smem, THREADS);
         __syncthreads();
         const uint32_t next = smisc[1];
 #else
@@ -609,6 +620,7 @@ __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS)
         // take the next ticket only now, so no tile waits on a held ticket
         __syncthreads();
         if (tid == 0) smisc[1] = atomicAdd(p.ticket, 1u);
+        zero_counters<S>(smem, THREADS);
         __syncthreads();
         tile = smisc[1];
         if (tile >= p.num_tiles) break;
@@ -726,6 +738,7 @@ __device__ __forceinline__ void downsweep_tile(const PassParams& p, unsigned cha
         running += cnt;
     }
     __syncthreads();
+    zero_counters<S>(smem, THREADS);  // for the next tile; the scatter does not read them
     tile_scatter<FULL, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile);
     __syncthreads();  // the next tile reuses shared memory
 }
@@ -740,6 +753,7 @@ __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS)
     uint32_t* sscan = reinterpret_cast<uint32_t*>(smem + S::scan_off);
     const int tid = threadIdx.x;
     const uint32_t g = blockIdx.x;
+    zero_counters<S>(smem, THREADS);  // made visible by the scan's barriers
     const uint32_t dstart = bins_exclusive_scan<BINS>(tid < BINS ? p.ghist[tid] : 0u, sscan, nullptr);
     uint32_t running = tid < BINS ? dstart + p.counts[(size_t)tid * p.G + g] : 0u;
     const uint32_t t0 = g * p.tiles_per_cta;
