@@ -77,8 +77,8 @@ typedef enum rs_status {
 typedef enum rs_key_type { RS_U32 = 0, RS_I32 = 1, RS_F32 = 2, RS_U64 = 3 } rs_key_type;
 
 typedef enum rs_algo {
-    RS_ALGO_AUTO = 0,        /* reduce-then-scan for 32-bit keys-only n >= 2^25 and
-                                for n >= 2^30; the chained scan otherwise        */
+    RS_ALGO_AUTO = 0,        /* reduce-then-scan for n >= 2^25, the chained scan
+                                below (both measured on GB300)                   */
     RS_ALGO_ONESWEEP = 1,    /* one upfront histogram read + one kernel per pass    */
     RS_ALGO_REDUCE_SCAN = 2  /* upsweep + spine scan + downsweep per pass           */
 } rs_algo;

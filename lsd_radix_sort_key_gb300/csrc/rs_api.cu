@@ -69,10 +69,10 @@ rs_status make_plan(const rs_sort_desc* d, rs::Plan* pl)
     pl->passes = rs::passes_for(d->begin_bit, d->end_bit, pl->radix_bits);
     pl->algo = d->algo;
     if (pl->algo == RS_ALGO_AUTO) {
-        // Chosen by measurement on GB300: reduce-then-scan is faster for large
-        // 32-bit keys-only sorts, the chained scan for everything else (and it
-        // needs n < 2^30).
-        const bool rts = n > kOnesweepMaxN || (!vals && kb == 4 && n >= kAutoReduceScanMinN);
+        // Chosen by measurement on GB300: reduce-then-scan is faster from 2^25
+        // keys for every key type, with or without values; the chained scan
+        // (fewer launches) below that.  The chained scan needs n < 2^30.
+        const bool rts = n > kOnesweepMaxN || n >= kAutoReduceScanMinN;
         pl->algo = rts ? RS_ALGO_REDUCE_SCAN : RS_ALGO_ONESWEEP;
     }
     if (pl->algo == RS_ALGO_ONESWEEP && n > kOnesweepMaxN) return RS_ERR_UNSUPPORTED;

@@ -27,9 +27,17 @@ constexpr int kRtsMaxCtas = 4096;
 // bytes, has values) so that keys, packed ranks and values stay in registers
 // at 1024 resident threads per SM (64 registers each).  The chained-scan pass
 // uses larger tiles than the reduce-then-scan downsweep: fewer tiles mean a
-// shorter look-back and less status traffic.  (Measured on 2^28 uint32 keys.)
+// shorter look-back and less status traffic; the downsweep uses 512 threads
+// when values ride along or keys are 64-bit (longer digit runs per tile).
+// (All measured on 2^28 keys.)
 #ifndef RS_RTS_THREADS
 #define RS_RTS_THREADS 256
+#endif
+#ifndef RS_RTS_THREADS_PAIRS
+#define RS_RTS_THREADS_PAIRS 512
+#endif
+#ifndef RS_RTS_THREADS_U64
+#define RS_RTS_THREADS_U64 512
 #endif
 #ifndef RS_OS_THREADS
 #define RS_OS_THREADS 512
@@ -38,7 +46,13 @@ constexpr int kRtsMaxCtas = 4096;
 #define RS_ITEMS_U32_KEYS 16
 #endif
 enum : int { kAlgoOnesweep = 1, kAlgoReduceScan = 2 };
-constexpr int tile_threads(int algo) { return algo == kAlgoOnesweep ? RS_OS_THREADS : RS_RTS_THREADS; }
+constexpr int tile_threads(int algo, int key_bytes, bool vals)
+{
+    return algo == kAlgoOnesweep ? RS_OS_THREADS
+           : key_bytes == 8      ? RS_RTS_THREADS_U64
+           : vals                ? RS_RTS_THREADS_PAIRS
+                                 : RS_RTS_THREADS;
+}
 #ifndef RS_ITEMS_U32_PAIRS
 #define RS_ITEMS_U32_PAIRS 12
 #endif
@@ -48,7 +62,7 @@ constexpr int tile_items(int key_bytes, bool vals)
 }
 constexpr int tile_keys(int algo, int key_bytes, bool vals)
 {
-    return tile_threads(algo) * tile_items(key_bytes, vals);
+    return tile_threads(algo, key_bytes, vals) * tile_items(key_bytes, vals);
 }
 
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

@@ -72,6 +72,23 @@
 #ifndef RS_CHAINS
 #define RS_CHAINS 1
 #endif
+//   RS_RANK_ATOMIC  1: one leader lane per digit advances the counter with a
+//                   shared atomic and hands the old count to its peers with a
+//                   shuffle; 0: every lane reads the counter and the peers
+//                   store the advanced count.
+#ifndef RS_RANK_ATOMIC
+#define RS_RANK_ATOMIC 0
+#endif
+//   RS_LOAD_STREAM  1: tile loads are streaming (evict-first) loads.
+//   RS_STORE_KEEP   1: scatter stores carry an L2 evict-last policy, so lines
+//                   that a digit run leaves half written stay resident until
+//                   the next tile completes them.
+#ifndef RS_LOAD_STREAM
+#define RS_LOAD_STREAM 0
+#endif
+#ifndef RS_STORE_KEEP
+#define RS_STORE_KEEP 1
+#endif
 //   RS_OS_PERSISTENT   1: chained-scan CTAs loop over tiles and prefetch the
 //                   next one; 0: one tile per CTA.
 #ifndef RS_OS_PERSISTENT
@@ -153,6 +170,23 @@ __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p)
 __device__ __forceinline__ void st_relaxed_gpu(uint32_t* p, uint32_t v)
 {
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// A 64-bit L2 cache policy that marks lines evict-last.
+__device__ __forceinline__ uint64_t l2_evict_last_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+template <typename T>
+__device__ __forceinline__ void st_keep(T* addr, T v, uint64_t pol)
+{
+    if constexpr (sizeof(T) == 8)
+        asm volatile("st.global.L2::cache_hint.b64 [%0], %1, %2;" ::"l"(addr), "l"(v), "l"(pol) : "memory");
+    else
+        asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(addr), "r"(v), "l"(pol) : "memory");
 }
 
 __device__ __forceinline__ uint32_t lanemask_lt()
@@ -253,8 +287,13 @@ __device__ __forceinline__ void load_striped(const T* __restrict__ src, uint32_t
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
         const uint32_t i = seg + k * 32 + lane;
+#if RS_LOAD_STREAM
+        if (FULL) v[k] = __ldcs(src + i);
+        else v[k] = i < n ? __ldcs(src + i) : T(0);
+#else
         if (FULL) v[k] = src[i];
         else v[k] = i < n ? src[i] : T(0);
+#endif
     }
 }
 
@@ -334,8 +373,15 @@ __device__ __forceinline__ void rank_in_warp(const typename KeyOps<KT>::T (&key)
             uint32_t* cnt = wh + c * WH;
             const uint32_t d = step_digit<FULL, KT, RB, ITEMS>(key, k, seg, n, shift, mask, lane);
             const uint32_t peers = warp_peers<FULL ? RB : RB + 1, RB>(d);
+#if RS_RANK_ATOMIC
+            const int leader = 31 - __clz(peers);
+            uint32_t old = 0;
+            if (leader == lane) old = atomicAdd(cnt + d, (uint32_t)__popc(peers));
+            const uint32_t prior = __shfl_sync(0xFFFFFFFFu, old, leader);
+#else
             const uint32_t prior = cnt[d];
             cnt[d] = prior + __popc(peers);
+#endif
             const uint32_t r = prior + __popc(peers & lt);
             rank[k / 2] |= (k & 1) ? (r << 16) : r;
         }
@@ -446,6 +492,9 @@ __device__ __forceinline__ void tile_scatter(const PassParams& p, unsigned char*
     const uint32_t tile_base = tile * (uint32_t)TILE;
     const uint32_t valid = FULL ? (uint32_t)TILE : p.n - tile_base;
     uint32_t bad = 0;
+#if RS_STORE_KEEP
+    const uint64_t pol = l2_evict_last_policy();
+#endif
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
         const uint32_t s = (uint32_t)(k * THREADS) + threadIdx.x;
@@ -455,8 +504,13 @@ __device__ __forceinline__ void tile_scatter(const PassParams& p, unsigned char*
             const bool ok = idx < p.n;
             bad |= !ok;
             if (ok) {
+#if RS_STORE_KEEP
+                st_keep(out + idx, kk, pol);
+                if constexpr (VALS) st_keep(p.vals_out + idx, svals[s], pol);
+#else
                 out[idx] = kk;
                 if constexpr (VALS) p.vals_out[idx] = svals[s];
+#endif
             }
         }
     }
@@ -969,7 +1023,7 @@ rs_status run_passes(Plan& pl)
     base.stall_tile = pl.stall_tile;
 
     if (pl.algo == RS_ALGO_ONESWEEP) {
-        constexpr int THREADS = tile_threads(kAlgoOnesweep);
+        constexpr int THREADS = tile_threads(kAlgoOnesweep, KB, VALS);
         constexpr int TILE = THREADS * ITEMS;
         using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
         const uint32_t num_tiles = (n + TILE - 1) / TILE;
@@ -1028,7 +1082,7 @@ rs_status run_passes(Plan& pl)
     }
 
     // Reduce-then-scan.
-    constexpr int THREADS = tile_threads(kAlgoReduceScan);
+    constexpr int THREADS = tile_threads(kAlgoReduceScan, KB, VALS);
     constexpr int TILE = THREADS * ITEMS;
     using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
     const uint32_t num_tiles = (n + TILE - 1) / TILE;

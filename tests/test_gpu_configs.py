@@ -48,8 +48,8 @@ def test_chained_scan_full_size():
     run_workload(synth.WORKLOADS["c4a_u32_2p28"], algo="onesweep")
 
 
-def test_reduce_then_scan_pairs_full_size():
-    run_workload(synth.WORKLOADS["c4b_morton_2p28"], algo="reduce_scan")
+def test_chained_scan_pairs_full_size():
+    run_workload(synth.WORKLOADS["c4b_morton_2p28"], algo="onesweep")
 
 
 def test_sweep_largest_size():
