@@ -355,6 +355,24 @@ def run_ours(args):
         "clocks": clk,
     }
 
+    # The same sort replayed as one CUDA graph (rs_graph_*): no host launch
+    # cost between kernels; reported beside the profiled value.
+    graph = rs.Graph(desc)
+    for _ in range(3):
+        graph.launch(stream)
+    torch.cuda.synchronize(dev)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(args.steps):
+        graph.launch(stream)
+    g1.record(stream)
+    torch.cuda.synchronize(dev)
+    graph_ms = max_over_ranks(pg, g0.elapsed_time(g1), dev) / args.steps
+    graph.close()
+    assert rs.rs_device_status(temp, stream) == 0
+    line["graph"] = {"value": round(n * ws / (graph_ms * 1e-3) / 1e9, 3), "unit": "Gkeys/s",
+                     "ms_per_step": round(graph_ms, 4), "api": "rs_graph_create / rs_graph_launch"}
+
     # End to end through the C ABI with host buffers.
     if not args.no_e2e:
         host_ko = torch.empty_like(host_k).pin_memory()
