@@ -29,6 +29,15 @@
  * scan with decoupled look-back that reads every key once up front for all
  * pass histograms.
  *
+ * Pass skipping.  The first read of the keys also records which bits of T(key)
+ * differ between keys and whether the input is already in order.  A pass
+ * whose digit is the same for every key, and every pass of an input already
+ * in order ("高性能计算：GPU上的基数排序", section 基数排序在GPU上的具体实现),
+ * is skipped on the device: its kernels still launch (the launch sequence
+ * depends on the shape only, so a captured graph stays valid) but return at
+ * once, and the remaining passes re-route their buffers so the result still
+ * lands in keys_out.  The output is the same as without skipping.
+ *
  * Conventions for every entry point below.
  *   Pointers.  Key, value and temp pointers are DEVICE pointers (cudaMalloc,
  *     cudaMallocAsync or a framework allocator) unless a parameter says
@@ -37,9 +46,10 @@
  *   Alignment.  Keys and values must be aligned to their element size; temp
  *     must be 256-byte aligned.  16-byte-aligned keys take the vector-load
  *     path; others are still sorted correctly.
- *   Aliasing.  keys_out may equal keys_in exactly (in-place sort; an odd pass
- *     count then costs one extra copy), likewise vals_out and vals_in.  Any
- *     other overlap among the key, value and temp buffers is RS_ERR_ALIAS.
+ *   Aliasing.  keys_out may equal keys_in exactly (in-place sort: one more
+ *     kernel is launched, which copies the result back from temp when an odd
+ *     number of passes ran), likewise vals_out and vals_in.  Any other
+ *     overlap among the key, value and temp buffers is RS_ERR_ALIAS.
  *   Stream.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
  *     default stream).  Calls only enqueue work: they do not synchronise,
  *     allocate or read device memory back, so they may be captured into a
@@ -168,9 +178,24 @@ int rs_sort_kernel_count(const rs_sort_desc* desc);
  * Waits for `stream`, then reads and clears the device error word in `temp`
  * (the last sort enqueued with this temp on this stream).  Returns RS_OK,
  * RS_ERR_DEVICE_TIMEOUT, RS_ERR_CHECK_FAILED, or RS_ERR_CUDA if the wait or
- * the copy fails.  This is the only entry point that synchronises.
+ * the copy fails.  This and rs_skip_record are the only entry points that
+ * synchronise.
  */
 rs_status rs_device_status(const void* temp, void* stream);
+
+/*
+ * Waits for `stream`, then reads the pass-skip record that the last sort
+ * enqueued with this temp on this stream left in it (see "Pass skipping"
+ * above): *differing_bits = the OR over all keys of T(key) ^ T(keys[0]), so a
+ * clear bit is one that every key shares (the high 32 bits are 0 for 32-bit
+ * keys); *unordered = 1 if some adjacent pair of keys is out of order in
+ * [begin_bit, end_bit), 0 if the input was already sorted (then no pass ran).
+ * A pass ran iff unordered and its digit's bits are not all clear.  The
+ * record is meaningful after a sort with n > 0 and begin_bit < end_bit.
+ * Returns RS_ERR_INVALID_ARG for a NULL pointer, RS_ERR_CUDA if the copy or
+ * the wait fails.
+ */
+rs_status rs_skip_record(const void* temp, void* stream, uint64_t* differing_bits, int* unordered);
 
 /* Static English text for a status code; never NULL. */
 const char* rs_status_string(rs_status status);

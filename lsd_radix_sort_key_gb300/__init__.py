@@ -59,6 +59,7 @@ SIGNATURES = {
                               ctypes.POINTER(_i), ctypes.POINTER(_i)]),
     "rs_sort_kernel_count": (_i, [ctypes.POINTER(SortDesc)]),
     "rs_device_status": (_i, [_vp, _vp]),
+    "rs_skip_record": (_i, [_vp, _vp, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(_i)]),
     "rs_status_string": (ctypes.c_char_p, [_i]),
     "rs_graph_create": (_i, [ctypes.POINTER(SortDesc), ctypes.POINTER(_vp)]),
     "rs_graph_launch": (_i, [_vp, _vp]),
@@ -189,6 +190,13 @@ def rs_sort_profiled(desc: SortDesc, events):
 
 def rs_device_status(temp, stream=None) -> int:
     return lib().rs_device_status(_addr(temp), _stream(stream))
+
+
+def rs_skip_record(temp, stream=None):
+    """(status, differing_bits, unordered) of the last sort that used temp."""
+    bits, unordered = ctypes.c_uint64(0), _i(0)
+    st = lib().rs_skip_record(_addr(temp), _stream(stream), ctypes.byref(bits), ctypes.byref(unordered))
+    return st, bits.value, unordered.value
 
 
 def rs_sort_host(key_type, h_keys_in, h_keys_out, h_vals_in, h_vals_out, n, begin_bit, end_bit,

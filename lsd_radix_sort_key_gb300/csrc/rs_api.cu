@@ -259,6 +259,19 @@ rs_status rs_device_status(const void* temp, void* stream)
     return RS_OK;
 }
 
+rs_status rs_skip_record(const void* temp, void* stream, uint64_t* differing_bits, int* unordered)
+{
+    if (!temp || !differing_bits || !unordered) return RS_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint32_t* rec = reinterpret_cast<const uint32_t*>(temp) + rs::kSkipBase;
+    uint32_t w[3] = {0, 0, 0};
+    if (cudaMemcpyAsync(w, rec, sizeof(w), cudaMemcpyDeviceToHost, s) != cudaSuccess) return RS_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return RS_ERR_CUDA;
+    *differing_bits = ((uint64_t)w[1] << 32) | w[0];
+    *unordered = w[2] != 0u ? 1 : 0;
+    return RS_OK;
+}
+
 const char* rs_status_string(rs_status status)
 {
     switch (status) {

@@ -13,10 +13,18 @@ namespace rs {
 // Largest number of digit passes any request can need (64-bit keys, 4-bit digits).
 constexpr int kMaxPasses = 16;
 
-// The "meta" block at the start of temp: the device error word, one tile
-// ticket per pass (chained scan) and one 256-bin global histogram per pass.
+// The "meta" block at the start of temp: the device error word; the pass-skip
+// record written by the first read of the keys (words kSkipBase..+3: the OR
+// over all keys of ordered(key) ^ ordered(keys[0]) as two 32-bit halves, a
+// flag set when some adjacent pair is out of order, and a count of the CTAs
+// that have added their share); one tile ticket per pass (chained scan); the
+// pass plan the last of those CTAs derives from the record (one word per
+// pass: runs | index among running passes << 8 | running passes << 16); and
+// one 256-bin global histogram per pass.
 constexpr int kErrWord = 0;
+constexpr int kSkipBase = 4;
 constexpr int kTicketBase = 16;
+constexpr int kPlanBase = 32;
 constexpr int kGhistBase = 64;
 constexpr int kMetaWords = kGhistBase + kMaxPasses * 256;
 

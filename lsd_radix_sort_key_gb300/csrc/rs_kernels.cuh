@@ -23,6 +23,14 @@
 //   * reduce-then-scan (k_upsweep, k_spine_scan, k_downsweep per pass): each
 //     CTA owns a contiguous chunk of tiles; the spine scan is step 2 proper.
 //
+// Pass skipping: the first read of the keys (k_histogram, or the first
+// k_upsweep) also records which key bits differ between keys and whether the
+// input is already in order, and its last CTA turns that into a plan of
+// which passes run.  Every later kernel reads the plan: a pass whose digit is
+// the same for every key, or every pass of an input already in order, returns
+// at once, and the running passes take their buffers from the plan so that
+// the result still lands in keys_out (section "pass skipping" below).
+//
 // Keys are carried with their original bit patterns.  The order-preserving
 // map T (identity, sign flip for int32, the NaN/Inf-aware flip for float32)
 // is applied when a digit is extracted, in every pass -- as the CPU code of
@@ -88,11 +96,6 @@
 #endif
 #ifndef RS_STORE_KEEP
 #define RS_STORE_KEEP 1
-#endif
-//   RS_OS_PERSISTENT   1: chained-scan CTAs loop over tiles and prefetch the
-//                   next one; 0: one tile per CTA.
-#ifndef RS_OS_PERSISTENT
-#define RS_OS_PERSISTENT 0
 #endif
 
 namespace rs {
@@ -236,10 +239,26 @@ __device__ __forceinline__ uint32_t bins_exclusive_scan(uint32_t v, uint32_t* sc
 // ------------------------------------------------------------ pass parameters
 
 struct PassParams {
+    // This pass's source and destination when every pass runs (the host's
+    // plan); when the skip record drops a pass, the kernels work out the
+    // actual ones from the sort-level buffers below (pass_buffers).
     const void* keys_in;
     void* keys_out;
     const uint32_t* vals_in;
     uint32_t* vals_out;
+    const void* sort_keys_in;   // the sort's input and output
+    void* sort_keys_out;
+    const uint32_t* sort_vals_in;
+    uint32_t* sort_vals_out;
+    void* alt_keys;          // the ping-pong partner buffers in temp
+    uint32_t* alt_vals;
+    uint32_t* skip;          // the skip record in temp (see kSkipBase)
+    uint32_t* plan;          // the pass plan in temp (see kPlanBase)
+    uint32_t pass;           // this pass's index and the geometry of all passes
+    uint32_t passes;
+    uint32_t begin_bit;
+    uint32_t end_bit;
+    uint32_t in_place;       // keys_in == keys_out
     uint32_t n;
     uint32_t shift;          // lowest bit of this pass's digit in the ordered key
     uint32_t mask;           // digit mask (fewer bits on a final partial digit)
@@ -272,8 +291,214 @@ struct TileSmem {
     static constexpr size_t base_off = wh_off + align_up(4 * (size_t)VWARPS * WH, 16);
     static constexpr size_t scan_off = base_off + 4 * BINS;
     static constexpr size_t misc_off = scan_off + 4 * 32;
-    static constexpr size_t bytes = misc_off + 16;
+    static constexpr size_t io_off = misc_off + 16;  // this pass's 4 buffer pointers
+    static constexpr size_t bytes = io_off + 32;
 };
+
+// ------------------------------------------------------------ pass skipping
+//
+// The first read of the keys (the first upsweep, or the all-pass histogram)
+// records two facts about the ordered keys in temp: `diff`, the OR over all
+// keys of ordered(key) ^ ordered(keys[0]), whose clear bits are the bits that
+// every key shares; and whether some adjacent pair is out of order in the
+// sorted bit range.  A pass whose digit bits are all clear in diff leaves every
+// key where it is (every key has the same digit and the pass is stable), so it
+// is skipped, and an input that is already in order skips every pass (the
+// early exit of "高性能计算：GPU上的基数排序", section 基数排序在GPU上的具体实现).
+// Every kernel of a pass reads the record itself, so the decision needs no
+// host round trip and a captured graph replays it.
+
+// The pass plan from the finished record: pass q runs iff the input is not
+// already in order and some bit of its digit differs between keys; its word
+// holds runs | j << 8 | E << 16 (j = running passes before it, E = all
+// running passes).
+template <int RB>
+__device__ __forceinline__ void write_plan(uint32_t diff_lo, uint32_t diff_hi, uint32_t unsorted,
+                                           uint32_t* plan, uint32_t passes, uint32_t begin_bit, uint32_t end_bit)
+{
+    const uint64_t diff = ((uint64_t)diff_hi << 32) | diff_lo;
+    uint32_t E = 0;
+    for (uint32_t q = 0; q < passes; ++q) {
+        const uint32_t shift = begin_bit + q * RB;
+        const uint32_t width = min((uint32_t)RB, end_bit - shift);
+        E += (unsorted != 0u && ((diff >> shift) & ((1ull << width) - 1ull)) != 0ull) ? 1u : 0u;
+    }
+    uint32_t j = 0;
+    for (uint32_t q = 0; q < passes; ++q) {
+        const uint32_t shift = begin_bit + q * RB;
+        const uint32_t width = min((uint32_t)RB, end_bit - shift);
+        const uint32_t run = (unsorted != 0u && ((diff >> shift) & ((1ull << width) - 1ull)) != 0ull) ? 1u : 0u;
+        plan[q] = run | (j << 8) | (E << 16);
+        j += run;
+    }
+}
+
+// One thread's share of the record.  The order check compares the ordered
+// keys masked to the sorted bit range in place (no shift needed: masking
+// keeps the order of the range's value); MASKED = false when the range is the
+// whole key.
+template <int KT, bool MASKED = true>
+struct SkipAcc {
+    using T = typename KeyOps<KT>::T;
+    T ref;          // ordered(keys[0])
+    T rmask;        // bits [begin_bit, end_bit)
+    T diff = 0;
+    bool unsorted = false;
+
+    __device__ __forceinline__ SkipAcc(const T* keys, uint32_t begin_bit, uint32_t end_bit)
+        : ref(KeyOps<KT>::ordered(keys[0])),
+          rmask(((end_bit - begin_bit >= 8 * sizeof(T)) ? ~T(0) : (T(1) << (end_bit - begin_bit)) - T(1))
+                << begin_bit) {}
+
+    // Folds one key into diff and returns its value for the order check.
+    __device__ __forceinline__ T visit(T k)
+    {
+        const T o = KeyOps<KT>::ordered(k);
+        diff |= o ^ ref;
+        return MASKED ? (o & rmask) : o;
+    }
+    __device__ __forceinline__ T value(T k) const
+    {
+        return MASKED ? (KeyOps<KT>::ordered(k) & rmask) : KeyOps<KT>::ordered(k);
+    }
+    __device__ __forceinline__ void pair(T a, T b) { unsorted |= a > b; }
+
+    // The keys of one 16-byte vector, checked in order; returns the values
+    // of the first and the last.
+    template <int VEC>
+    __device__ __forceinline__ void vector(const T (&k)[VEC], T& first, T& last)
+    {
+        T prev = visit(k[0]);
+        first = prev;
+#pragma unroll
+        for (int j = 1; j < VEC; ++j) {
+            const T v = visit(k[j]);
+            pair(prev, v);
+            prev = v;
+        }
+        last = prev;
+    }
+
+    // Every thread of the block calls this once at the end, between two
+    // barriers: each warp ORs its share into the block's words `blk` (3
+    // words, zeroed before the first barrier); flush_block then adds the
+    // block's to the record with one atomic per word, so that the CTAs do not
+    // all queue on the record's line warp by warp.
+    __device__ __forceinline__ void flush_warp(uint32_t* blk)
+    {
+        const uint64_t d = (uint64_t)diff;
+        const uint32_t lo = __reduce_or_sync(0xFFFFFFFFu, (uint32_t)d);
+        const uint32_t hi = __reduce_or_sync(0xFFFFFFFFu, (uint32_t)(d >> 32));
+        const bool un = __any_sync(0xFFFFFFFFu, unsorted);
+        if ((threadIdx.x & 31) == 0) {
+            if (lo) atomicOr(blk + 0, lo);
+            if (hi) atomicOr(blk + 1, hi);
+            if (un) atomicOr(blk + 2, 1u);
+        }
+    }
+    // Thread 0 of the last CTA to add its share also writes the pass plan.
+    template <int RB>
+    static __device__ __forceinline__ void flush_block(const uint32_t* blk, uint32_t* skip, uint32_t* plan,
+                                                       uint32_t passes, uint32_t begin_bit, uint32_t end_bit)
+    {
+        if (threadIdx.x == 0) {
+            if (blk[0]) atomicOr(skip + 0, blk[0]);
+            if (blk[1]) atomicOr(skip + 1, blk[1]);
+            if (blk[2]) atomicOr(skip + 2, 1u);
+            __threadfence();
+            if (atomicAdd(skip + 3, 1u) == gridDim.x - 1) {
+                __threadfence();
+                write_plan<RB>(ld_relaxed_gpu(skip + 0), ld_relaxed_gpu(skip + 1), ld_relaxed_gpu(skip + 2),
+                               plan, passes, begin_bit, end_bit);
+            }
+        }
+    }
+};
+
+// Which passes run: `run` for this pass, `j` = how many running passes come
+// before it, `E` = how many run in all.
+struct PassRole {
+    bool run;
+    uint32_t j;
+    uint32_t E;
+};
+
+__device__ __forceinline__ PassRole decode_plan(uint32_t w)
+{
+    return PassRole{(w & 1u) != 0u, (w >> 8) & 0xFFu, (w >> 16) & 0xFFu};
+}
+
+// This pass's plan word, read by one thread per CTA.
+__device__ __forceinline__ uint32_t load_plan(const PassParams& p) { return p.plan[p.pass]; }
+
+struct RoleShared {
+    uint32_t run, j, E;
+};
+
+__device__ __forceinline__ void publish_role(RoleShared* sh, const PassRole& r)
+{
+    sh->run = r.run ? 1u : 0u;
+    sh->j = r.j;
+    sh->E = r.E;
+}
+
+__device__ __forceinline__ PassRole read_role(const RoleShared* sh)
+{
+    return PassRole{sh->run != 0u, sh->j, sh->E};
+}
+
+// Thread 0 reads the plan; every thread returns it (holds a barrier).
+__device__ __forceinline__ PassRole block_pass_role(const PassParams& p, RoleShared* sh)
+{
+    if (threadIdx.x == 0) publish_role(sh, decode_plan(load_plan(p)));
+    __syncthreads();
+    return read_role(sh);
+}
+
+// Buffer i of the chain of running passes: i = 0 is the sort's input.  Out of
+// place, buffers 1..E alternate so that buffer E is keys_out.  In place, even
+// i is keys_out (= keys_in) and odd i the partner, so with E odd the result
+// ends in the partner and k_chain_copy moves it back.  (The host plans the
+// every-pass-runs case with the same rule.)
+__host__ __device__ __forceinline__ bool chain_is_out(uint32_t i, uint32_t E, bool in_place)
+{
+    return in_place ? (i % 2u == 0u) : ((E - i) % 2u == 0u);
+}
+
+// This pass's source and destination for role r.
+template <bool VALS>
+__device__ __forceinline__ void pass_buffers(PassParams& p, const PassRole& r)
+{
+    const bool ip = p.in_place != 0u;
+    const bool src_out = chain_is_out(r.j, r.E, ip), dst_out = chain_is_out(r.j + 1, r.E, ip);
+    p.keys_in = r.j == 0 ? p.sort_keys_in : (src_out ? p.sort_keys_out : p.alt_keys);
+    p.keys_out = dst_out ? p.sort_keys_out : p.alt_keys;
+    if constexpr (VALS) {
+        p.vals_in = r.j == 0 ? p.sort_vals_in : (src_out ? p.sort_vals_out : p.alt_vals);
+        p.vals_out = dst_out ? p.sort_vals_out : p.alt_vals;
+    }
+}
+
+// Copy elements [lo, hi) of the keys (and values), thread t of `stride`.
+template <typename T, bool VALS>
+__device__ __forceinline__ void copy_span(const T* src, T* dst, const uint32_t* vsrc, uint32_t* vdst,
+                                          size_t lo, size_t hi, size_t t, size_t stride)
+{
+    for (size_t i = lo + t; i < hi; i += stride) {
+        dst[i] = src[i];
+        if constexpr (VALS) vdst[i] = vsrc[i];
+    }
+}
+
+// When no pass runs, the last pass's kernel copies the input to the output
+// (out of place); its CTAs cover [lo, hi) each.
+template <typename T, bool VALS>
+__device__ __forceinline__ void copy_if_no_pass_runs(const PassParams& p, const PassRole& r, size_t lo, size_t hi)
+{
+    if (r.E == 0u && p.pass + 1u == p.passes && p.in_place == 0u)
+        copy_span<T, VALS>(static_cast<const T*>(p.sort_keys_in), static_cast<T*>(p.sort_keys_out),
+                           p.sort_vals_in, p.sort_vals_out, lo, hi < p.n ? hi : p.n, threadIdx.x, blockDim.x);
+}
 
 // --------------------------------------------------------------- tile pieces
 
@@ -297,23 +522,80 @@ __device__ __forceinline__ void load_striped(const T* __restrict__ src, uint32_t
     }
 }
 
+// When a pass was skipped, the buffers of the passes after it live in shared
+// memory (PassIO, written once per CTA by set_pass_io) rather than in
+// registers, which the tile loop has none to spare for; each use reloads them.
+struct PassIO {
+    const void* keys_in;
+    void* keys_out;
+    const uint32_t* vals_in;
+    uint32_t* vals_out;
+};
+
+__device__ __forceinline__ void* lds_ptr(const void* slot)
+{
+    uint64_t v;
+    asm volatile("ld.volatile.shared.u64 %0, [%1];"
+                 : "=l"(v)
+                 : "r"((uint32_t)__cvta_generic_to_shared(slot)));
+    return reinterpret_cast<void*>(v);
+}
+
+template <typename S>
+__device__ __forceinline__ void set_pass_io(unsigned char* smem, const PassParams& p)
+{
+    if (threadIdx.x == 0) {
+        PassIO* io = reinterpret_cast<PassIO*>(smem + S::io_off);
+        io->keys_in = p.keys_in;
+        io->keys_out = p.keys_out;
+        io->vals_in = p.vals_in;
+        io->vals_out = p.vals_out;
+    }
+}
+
+template <typename S, typename T>
+__device__ __forceinline__ const T* io_keys_in(const unsigned char* smem)
+{
+    return static_cast<const T*>(lds_ptr(&reinterpret_cast<const PassIO*>(smem + S::io_off)->keys_in));
+}
+template <typename S, typename T>
+__device__ __forceinline__ T* io_keys_out(const unsigned char* smem)
+{
+    return static_cast<T*>(lds_ptr(&reinterpret_cast<const PassIO*>(smem + S::io_off)->keys_out));
+}
+template <typename S>
+__device__ __forceinline__ const uint32_t* io_vals_in(const unsigned char* smem)
+{
+    return static_cast<const uint32_t*>(lds_ptr(&reinterpret_cast<const PassIO*>(smem + S::io_off)->vals_in));
+}
+template <typename S>
+__device__ __forceinline__ uint32_t* io_vals_out(const unsigned char* smem)
+{
+    return static_cast<uint32_t*>(lds_ptr(&reinterpret_cast<const PassIO*>(smem + S::io_off)->vals_out));
+}
+
 // Keys (and values) of one tile in warp-striped order; a tile that runs past
-// n is guarded lane by lane.
-template <int KT, int THREADS, int ITEMS, bool VALS>
-__device__ __forceinline__ void load_tile(const PassParams& p, uint32_t tile,
+// n is guarded lane by lane.  The source is the pass's planned buffer
+// (p.keys_in), or with DYN the one in the PassIO slots.
+template <int KT, int RB, int THREADS, int ITEMS, bool VALS, bool DYN>
+__device__ __forceinline__ void load_tile(const PassParams& p, const unsigned char* smem, uint32_t tile,
                                           typename KeyOps<KT>::T (&key)[ITEMS],
                                           uint32_t (&val)[VALS ? ITEMS : 1])
 {
     using T = typename KeyOps<KT>::T;
+    using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
     constexpr uint32_t TILE = THREADS * ITEMS;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t seg = tile * TILE + (uint32_t)warp * (32u * ITEMS);
+    const T* kin = DYN ? io_keys_in<S, T>(smem) : static_cast<const T*>(p.keys_in);
     if ((tile + 1) * TILE <= p.n) {
-        load_striped<true, T, ITEMS>(static_cast<const T*>(p.keys_in), seg, p.n, lane, key);
-        if constexpr (VALS) load_striped<true, uint32_t, ITEMS>(p.vals_in, seg, p.n, lane, val);
+        load_striped<true, T, ITEMS>(kin, seg, p.n, lane, key);
+        if constexpr (VALS)
+            load_striped<true, uint32_t, ITEMS>(DYN ? io_vals_in<S>(smem) : p.vals_in, seg, p.n, lane, val);
     } else {
-        load_striped<false, T, ITEMS>(static_cast<const T*>(p.keys_in), seg, p.n, lane, key);
-        if constexpr (VALS) load_striped<false, uint32_t, ITEMS>(p.vals_in, seg, p.n, lane, val);
+        load_striped<false, T, ITEMS>(kin, seg, p.n, lane, key);
+        if constexpr (VALS)
+            load_striped<false, uint32_t, ITEMS>(DYN ? io_vals_in<S>(smem) : p.vals_in, seg, p.n, lane, val);
     }
 }
 
@@ -480,7 +762,8 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
 // warp store covers few, contiguous segments.  Positions are bounds-checked
 // (a failure is recorded and the store skipped).
 template <bool FULL, int KT, int RB, int THREADS, int ITEMS, bool VALS>
-__device__ __forceinline__ void tile_scatter(const PassParams& p, unsigned char* smem, uint32_t tile)
+__device__ __forceinline__ void tile_scatter(const PassParams& p, unsigned char* smem, uint32_t tile,
+                                             typename KeyOps<KT>::T* out, uint32_t* vout)
 {
     using T = typename KeyOps<KT>::T;
     using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
@@ -488,7 +771,6 @@ __device__ __forceinline__ void tile_scatter(const PassParams& p, unsigned char*
     const T* skeys = reinterpret_cast<const T*>(smem + S::keys_off);
     const uint32_t* svals = reinterpret_cast<const uint32_t*>(smem + S::vals_off);
     const uint32_t* sbase = reinterpret_cast<const uint32_t*>(smem + S::base_off);
-    T* out = static_cast<T*>(p.keys_out);
     const uint32_t tile_base = tile * (uint32_t)TILE;
     const uint32_t valid = FULL ? (uint32_t)TILE : p.n - tile_base;
     uint32_t bad = 0;
@@ -506,10 +788,10 @@ __device__ __forceinline__ void tile_scatter(const PassParams& p, unsigned char*
             if (ok) {
 #if RS_STORE_KEEP
                 st_keep(out + idx, kk, pol);
-                if constexpr (VALS) st_keep(p.vals_out + idx, svals[s], pol);
+                if constexpr (VALS) st_keep(vout + idx, svals[s], pol);
 #else
                 out[idx] = kk;
-                if constexpr (VALS) p.vals_out[idx] = svals[s];
+                if constexpr (VALS) vout[idx] = svals[s];
 #endif
             }
         }
@@ -590,13 +872,11 @@ __device__ __forceinline__ uint32_t lookback(const PassParams& p, uint32_t tile,
 
 // ------------------------------------------------------------------ kernels
 
-// One tile of a chained-scan pass.  `next` is the ticket this CTA already
-// holds for its following tile; that tile's keys are loaded into the freed
-// registers while this tile looks back and scatters.
+// One tile of a chained-scan pass.
 template <bool FULL, int KT, int RB, int THREADS, int ITEMS, bool VALS>
 __device__ __forceinline__ void onesweep_tile(const PassParams& p, unsigned char* smem, uint32_t tile,
-                                              uint32_t next, typename KeyOps<KT>::T (&key)[ITEMS],
-                                              uint32_t (&val)[VALS ? ITEMS : 1])
+                                              const typename KeyOps<KT>::T (&key)[ITEMS],
+                                              const uint32_t (&val)[VALS ? ITEMS : 1])
 {
     using T = typename KeyOps<KT>::T;
     using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
@@ -622,8 +902,6 @@ __device__ __forceinline__ void onesweep_tile(const PassParams& p, unsigned char
             }
             if (tile > 0) lookback_preload<RS_LOOKBACK_BATCH>(p, tile, d, BINS, pre);
         });
-    if (next < p.num_tiles) load_tile<KT, THREADS, ITEMS, VALS>(p, next, key, val);
-
     if (tid < BINS) {
         uint32_t excl = gexcl;
         if (tile > 0) {
@@ -632,14 +910,14 @@ __device__ __forceinline__ void onesweep_tile(const PassParams& p, unsigned char
         }
         sbase[tid] = excl - start;
     }
+    T* out = io_keys_out<S, T>(smem);
+    uint32_t* vout = VALS ? io_vals_out<S>(smem) : nullptr;
     __syncthreads();
-    tile_scatter<FULL, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile);
+    tile_scatter<FULL, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, out, vout);
 }
 
-// Chained-scan pass, persistent: each CTA takes tiles by an atomic ticket
-// until none is left.  Tickets are handed out in order, so every tile a CTA
-// waits on belongs to a CTA that already runs (and that CTA finishes the
-// tile it holds before the one it prefetches).
+// Chained-scan pass: one tile per CTA, in the order of an atomic ticket, so
+// every tile a CTA waits on belongs to a CTA that already runs.
 template <int KT, int RB, int THREADS, int ITEMS, bool VALS>
 __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS) k_onesweep(PassParams p)
 {
@@ -648,59 +926,65 @@ __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS)
     extern __shared__ __align__(16) unsigned char smem[];
     uint32_t* smisc = reinterpret_cast<uint32_t*>(smem + S::misc_off);
     const int tid = threadIdx.x;
-    if (tid == 0) smisc[0] = atomicAdd(p.ticket, 1u);
+    RoleShared* rsh = reinterpret_cast<RoleShared*>(smisc + 1);
+    if (tid == 0) {
+        // The skip record is read and the ticket taken together, so the two
+        // round trips overlap (a skipped pass leaves its tickets unused).
+        const uint32_t w = load_plan(p);
+        smisc[0] = atomicAdd(p.ticket, 1u);
+        const PassRole r = decode_plan(w);
+        publish_role(rsh, r);
+        if (r.run) {
+            PassParams q = p;
+            pass_buffers<VALS>(q, r);
+            set_pass_io<S>(smem, q);
+        }
+    }
     zero_counters<S>(smem, THREADS);
     __syncthreads();
-    uint32_t tile = smisc[0];
+    const PassRole role = read_role(rsh);
+    if (!role.run) {
+        const size_t lo = (size_t)blockIdx.x * S::TILE;
+        copy_if_no_pass_runs<T, VALS>(p, role, lo, lo + S::TILE);
+        return;
+    }
+    const uint32_t tile = smisc[0];
     if (tile >= p.num_tiles) return;
     T key[ITEMS];
     uint32_t val[VALS ? ITEMS : 1];
-    load_tile<KT, THREADS, ITEMS, VALS>(p, tile, key, val);
-    while (true) {
-#if RS_OS_PERSISTENT == 1
-        __syncthreads();  // the previous tile's scatter is done with shared memory
-        if (tid == 0) smisc[1] = atomicAdd(p.ticket, 1u);
-        zero_counters<S>(smem, THREADS);
-        __syncthreads();
-        const uint32_t next = smisc[1];
-#else
-        const uint32_t next = 0xFFFFFFFFu;
-#endif
-        if ((tile + 1) * (uint32_t)S::TILE <= p.n)
-            onesweep_tile<true, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, next, key, val);
-        else
-            onesweep_tile<false, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, next, key, val);
-#if RS_OS_PERSISTENT == 2
-        // take the next ticket only now, so no tile waits on a held ticket
-        __syncthreads();
-        if (tid == 0) smisc[1] = atomicAdd(p.ticket, 1u);
-        zero_counters<S>(smem, THREADS);
-        __syncthreads();
-        tile = smisc[1];
-        if (tile >= p.num_tiles) break;
-        load_tile<KT, THREADS, ITEMS, VALS>(p, tile, key, val);
-#else
-        if (next >= p.num_tiles) break;
-        tile = next;
-#endif
-    }
+    load_tile<KT, RB, THREADS, ITEMS, VALS, true>(p, smem, tile, key, val);
+    if ((tile + 1) * (uint32_t)S::TILE <= p.n)
+        onesweep_tile<true, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, key, val);
+    else
+        onesweep_tile<false, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, key, val);
 }
 
 // Reduce-then-scan, step 1: digit histogram of each CTA's chunk, written
 // digit-major (counts[d * G + g]) so that one exclusive scan of the whole
 // array yields every (digit, CTA) start ("Radix sort paralelo sobre el scan",
 // section "Las tres fases de una pasada").
-template <int KT, int RB, int THREADS, int TILE>
+// The first upsweep (FIRST) also writes the pass-skip record; every later one
+// runs only if its pass does.
+template <int KT, int RB, int THREADS, int TILE, bool FIRST>
 __global__ void __launch_bounds__(THREADS) k_upsweep(PassParams p)
 {
     using T = typename KeyOps<KT>::T;
     constexpr int BINS = 1 << RB;
     constexpr int COLS = 32;          // lane-private counter columns: hist[bin][lane]
     constexpr int VEC = 16 / sizeof(T);
+    constexpr int U = 4;              // vectors in flight per thread
     __shared__ uint32_t hist[BINS * COLS];
-    const int tid = threadIdx.x;
-    const uint32_t col = tid & 31;
+    __shared__ RoleShared rsh;
+    __shared__ uint32_t skip_blk[3];
+    if constexpr (!FIRST) {
+        const PassRole role = block_pass_role(p, &rsh);
+        if (!role.run) return;
+        pass_buffers<false>(p, role);
+    }
+    const int tid = threadIdx.x, lane = tid & 31;
+    const uint32_t col = lane;
     for (int i = tid; i < BINS * COLS; i += THREADS) hist[i] = 0;
+    if (FIRST && tid < 3) skip_blk[tid] = 0;
     __syncthreads();
     const uint32_t g = blockIdx.x;
     const uint64_t lo64 = (uint64_t)g * p.tiles_per_cta * TILE;
@@ -709,36 +993,69 @@ __global__ void __launch_bounds__(THREADS) k_upsweep(PassParams p)
     const uint32_t hi = hi64 < p.n ? (uint32_t)hi64 : p.n;
     const T* src = static_cast<const T*>(p.keys_in);
     auto count = [&](T k) { atomicAdd(&hist[digit_of<KT>(k, p.shift, p.mask) * COLS + col], 1u); };
+    SkipAcc<KT> acc(src, p.begin_bit, p.end_bit);
     // lo is a multiple of TILE, so lo * sizeof(T) is 16-byte aligned whenever the base is.
     uint32_t i = lo;
     if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
-        constexpr int U = 4;
         const uint32_t nvec = (hi - lo) / VEC;
         const uint4* sv = reinterpret_cast<const uint4*>(src + lo);
-        uint32_t v = tid;
-        for (; v + (U - 1) * THREADS < nvec; v += U * THREADS) {
+        // Full rounds (U vectors per thread, the same trip count in every
+        // warp), then what is left.  Thread v + 1 holds the vector after
+        // thread v's, so a shuffle brings the next key for the order check.
+        const uint32_t per_round = U * THREADS, rounds = nvec / per_round;
+        for (uint32_t r = 0; r < rounds; ++r) {
             uint4 w[U];
+            T nb[FIRST ? U : 1];  // lane 31: the key after its vector, loaded with the round
 #pragma unroll
-            for (int u = 0; u < U; ++u) w[u] = __ldcs(sv + v + u * THREADS);
+            for (int u = 0; u < U; ++u) {
+                const uint32_t v = r * per_round + u * THREADS + tid;
+                w[u] = __ldcs(sv + v);
+                if constexpr (FIRST) nb[u] = (lane == 31 && v + 1 < nvec) ? src[lo + (v + 1) * VEC] : T(0);
+            }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 T k[VEC];
                 memcpy(k, &w[u], 16);
 #pragma unroll
                 for (int j = 0; j < VEC; ++j) count(k[j]);
+                if constexpr (FIRST) {
+                    const uint32_t v = r * per_round + u * THREADS + tid;
+                    T first, last;
+                    acc.vector(k, first, last);
+                    T next = __shfl_down_sync(0xFFFFFFFFu, first, 1);
+                    if (lane == 31) next = v + 1 < nvec ? acc.value(nb[u]) : last;
+                    acc.pair(last, next);
+                }
             }
         }
-        for (; v < nvec; v += THREADS) {
+        for (uint32_t v = rounds * per_round + tid; v < nvec; v += THREADS) {
             const uint4 w = __ldcs(sv + v);
             T k[VEC];
             memcpy(k, &w, 16);
 #pragma unroll
             for (int j = 0; j < VEC; ++j) count(k[j]);
+            if constexpr (FIRST) {
+                T first, last;
+                acc.vector(k, first, last);
+                if (v + 1 < nvec) acc.pair(last, acc.value(src[lo + (v + 1) * VEC]));
+            }
         }
         i = lo + nvec * VEC;
     }
-    for (i += tid; i < hi; i += THREADS) count(src[i]);
+    for (i += tid; i < hi; i += THREADS) {
+        const T k = src[i];
+        count(k);
+        if constexpr (FIRST) {
+            const T v = acc.visit(k);
+            if (i > 0) acc.pair(acc.value(src[i - 1]), v);
+        }
+    }
+    if constexpr (FIRST) {
+        if (tid == 0 && lo > 0 && lo < hi) acc.pair(acc.value(src[lo - 1]), acc.value(src[lo]));
+        acc.flush_warp(skip_blk);
+    }
     __syncthreads();
+    if constexpr (FIRST) SkipAcc<KT>::template flush_block<RB>(skip_blk, p.skip, p.plan, p.passes, p.begin_bit, p.end_bit);
     for (int d = tid; d < BINS; d += THREADS) {
         uint32_t c = 0;
 #pragma unroll 8
@@ -750,12 +1067,15 @@ __global__ void __launch_bounds__(THREADS) k_upsweep(PassParams p)
 // Reduce-then-scan, step 2: exclusive scan of the digit-major counts.  CTA d
 // scans row d (its G per-CTA counts) in place and writes the row total; the
 // downsweep adds the exclusive scan of the row totals (the digit starts).
-template <int THREADS>
-__global__ void __launch_bounds__(THREADS) k_spine_scan(uint32_t* counts, uint32_t G, uint32_t* row_total)
+template <int RB, int THREADS>
+__global__ void __launch_bounds__(THREADS) k_spine_scan(PassParams p, uint32_t* row_total)
 {
     __shared__ uint32_t sscan[32];
+    __shared__ RoleShared rsh;
+    if (!block_pass_role(p, &rsh).run) return;
     const int tid = threadIdx.x;
-    uint32_t* row = counts + (size_t)blockIdx.x * G;
+    const uint32_t G = p.G;
+    uint32_t* row = p.counts + (size_t)blockIdx.x * G;
     const uint32_t per = (G + THREADS - 1) / THREADS;
     const uint32_t lo = min(G, tid * per), hi = min(G, lo + per);
     uint32_t sum = 0;
@@ -772,7 +1092,7 @@ __global__ void __launch_bounds__(THREADS) k_spine_scan(uint32_t* counts, uint32
 
 // Reduce-then-scan, step 3: each CTA walks its chunk tile by tile, keeping a
 // running global offset per digit.
-template <bool FULL, int KT, int RB, int THREADS, int ITEMS, bool VALS>
+template <bool FULL, int KT, int RB, int THREADS, int ITEMS, bool VALS, bool DYN>
 __device__ __forceinline__ void downsweep_tile(const PassParams& p, unsigned char* smem, uint32_t tile,
                                                uint32_t next, uint32_t& running,
                                                typename KeyOps<KT>::T (&key)[ITEMS],
@@ -786,15 +1106,39 @@ __device__ __forceinline__ void downsweep_tile(const PassParams& p, unsigned cha
     uint32_t cnt, start;
     tile_rank_and_shuffle<FULL, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, key, val, &cnt, &start,
                                                                [](int, uint32_t) {});
-    if (next != 0xFFFFFFFFu) load_tile<KT, THREADS, ITEMS, VALS>(p, next, key, val);
+    if (next != 0xFFFFFFFFu) load_tile<KT, RB, THREADS, ITEMS, VALS, DYN>(p, smem, next, key, val);
+    T* out = DYN ? io_keys_out<S, T>(smem) : static_cast<T*>(p.keys_out);
+    uint32_t* vout = VALS ? (DYN ? io_vals_out<S>(smem) : p.vals_out) : nullptr;
     if (tid < BINS) {
         sbase[tid] = running - start;
         running += cnt;
     }
     __syncthreads();
     zero_counters<S>(smem, THREADS);  // for the next tile; the scatter does not read them
-    tile_scatter<FULL, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile);
+    tile_scatter<FULL, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, out, vout);
     __syncthreads();  // the next tile reuses shared memory
+}
+
+// The tile loop of one downsweep CTA.  DYN: the pass's buffers come from the
+// PassIO slots (some earlier pass was skipped) instead of the host's plan.
+template <int KT, int RB, int THREADS, int ITEMS, bool VALS, bool DYN>
+__device__ __forceinline__ void downsweep_loop(const PassParams& p, unsigned char* smem, uint32_t running)
+{
+    using T = typename KeyOps<KT>::T;
+    using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
+    const uint32_t t0 = blockIdx.x * p.tiles_per_cta;
+    const uint32_t t1 = min(p.num_tiles, t0 + p.tiles_per_cta);
+    if (t0 >= t1) return;
+    T key[ITEMS];
+    uint32_t val[VALS ? ITEMS : 1];
+    load_tile<KT, RB, THREADS, ITEMS, VALS, DYN>(p, smem, t0, key, val);
+    for (uint32_t tile = t0; tile < t1; ++tile) {
+        const uint32_t next = tile + 1 < t1 ? tile + 1 : 0xFFFFFFFFu;
+        if ((tile + 1) * (uint32_t)S::TILE <= p.n)
+            downsweep_tile<true, KT, RB, THREADS, ITEMS, VALS, DYN>(p, smem, tile, next, running, key, val);
+        else
+            downsweep_tile<false, KT, RB, THREADS, ITEMS, VALS, DYN>(p, smem, tile, next, running, key, val);
+    }
 }
 
 template <int KT, int RB, int THREADS, int ITEMS, bool VALS>
@@ -805,24 +1149,49 @@ __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS)
     constexpr int BINS = S::BINS;
     extern __shared__ __align__(16) unsigned char smem[];
     uint32_t* sscan = reinterpret_cast<uint32_t*>(smem + S::scan_off);
+    RoleShared* rsh = reinterpret_cast<RoleShared*>(smem + S::misc_off + 4);
     const int tid = threadIdx.x;
     const uint32_t g = blockIdx.x;
-    zero_counters<S>(smem, THREADS);  // made visible by the scan's barriers
-    const uint32_t dstart = bins_exclusive_scan<BINS>(tid < BINS ? p.ghist[tid] : 0u, sscan, nullptr);
-    uint32_t running = tid < BINS ? dstart + p.counts[(size_t)tid * p.G + g] : 0u;
-    const uint32_t t0 = g * p.tiles_per_cta;
-    const uint32_t t1 = min(p.num_tiles, t0 + p.tiles_per_cta);
-    if (t0 >= t1) return;
-    T key[ITEMS];
-    uint32_t val[VALS ? ITEMS : 1];
-    load_tile<KT, THREADS, ITEMS, VALS>(p, t0, key, val);
-    for (uint32_t tile = t0; tile < t1; ++tile) {
-        const uint32_t next = tile + 1 < t1 ? tile + 1 : 0xFFFFFFFFu;
-        if ((tile + 1) * (uint32_t)S::TILE <= p.n)
-            downsweep_tile<true, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, next, running, key, val);
-        else
-            downsweep_tile<false, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, next, running, key, val);
+    // This CTA's digit totals and block offsets are read while thread 0
+    // reads the skip record (for a skipped pass they are dropped).
+    const uint32_t total = tid < BINS ? p.ghist[tid] : 0u;
+    const uint32_t block_off = tid < BINS ? p.counts[(size_t)tid * p.G + g] : 0u;
+    if (tid == 0) {
+        const PassRole r = decode_plan(load_plan(p));
+        publish_role(rsh, r);
+        if (r.run && r.E != p.passes) {
+            PassParams q = p;
+            pass_buffers<VALS>(q, r);
+            set_pass_io<S>(smem, q);
+        }
     }
+    zero_counters<S>(smem, THREADS);
+    // The scan's barriers also publish the role, the PassIO slots and the zeroed counters.
+    const uint32_t dstart = bins_exclusive_scan<BINS>(total, sscan, nullptr);
+    const PassRole role = read_role(rsh);
+    if (!role.run) {
+        const size_t lo = (size_t)g * p.tiles_per_cta * S::TILE;
+        copy_if_no_pass_runs<T, VALS>(p, role, lo, lo + (size_t)p.tiles_per_cta * S::TILE);
+        return;
+    }
+    const uint32_t running = tid < BINS ? dstart + block_off : 0u;
+    if (role.E == p.passes)  // every pass runs: the host's plan holds
+        downsweep_loop<KT, RB, THREADS, ITEMS, VALS, false>(p, smem, running);
+    else
+        downsweep_loop<KT, RB, THREADS, ITEMS, VALS, true>(p, smem, running);
+}
+
+// In place with an odd number of running passes the result ends in the
+// partner buffer (see chain_is_out): copy it back to keys_out.
+template <int RB, typename T, bool VALS>
+__global__ void __launch_bounds__(256) k_chain_copy(PassParams p)
+{
+    __shared__ RoleShared rsh;
+    const PassRole role = block_pass_role(p, &rsh);
+    if (p.in_place == 0u || role.E % 2u == 0u) return;
+    copy_span<T, VALS>(static_cast<const T*>(p.alt_keys), static_cast<T*>(p.sort_keys_out), p.alt_vals,
+                       p.sort_vals_out, 0, p.n, (size_t)blockIdx.x * blockDim.x + threadIdx.x,
+                       (size_t)gridDim.x * blockDim.x);
 }
 
 // Chained scan, the one upfront read: the digit histograms of ALL passes,
@@ -838,13 +1207,15 @@ struct HistParams {
     uint4* zero;            // status region to clear
     size_t zero_vec4;       // its size in 16-byte words
     int aligned16;          // keys pointer is 16-byte aligned
+    uint32_t* skip;         // the pass-skip record
+    uint32_t* plan;         // the pass plan
 };
 
 // Counters are lane-private columns, hist[pass][bin][col] with col = lane %
 // COLS, so the COLS lanes of a warp that share no column hit distinct banks:
 // the shared atomics of one warp instruction do not conflict (the warps of
 // the CTA still share the columns, which the atomics make safe).
-template <int KT, int RB, int THREADS, int COLS>
+template <int KT, int RB, int THREADS, int COLS, bool FULLRANGE>
 __global__ void __launch_bounds__(THREADS) k_histogram(HistParams h)
 {
     using T = typename KeyOps<KT>::T;
@@ -853,10 +1224,12 @@ __global__ void __launch_bounds__(THREADS) k_histogram(HistParams h)
     constexpr int U = 4;  // vectors in flight per thread
     extern __shared__ __align__(16) unsigned char smem[];
     uint32_t* hist = reinterpret_cast<uint32_t*>(smem);
+    __shared__ uint32_t skip_blk[3];
     const int tid = threadIdx.x;
     const uint32_t col = tid % COLS;
     const uint32_t words = h.passes * BINS * COLS;
     for (uint32_t i = tid; i < words; i += THREADS) hist[i] = 0;
+    if (tid < 3) skip_blk[tid] = 0;
     __syncthreads();
 
     auto count = [&](T k) {
@@ -872,35 +1245,61 @@ __global__ void __launch_bounds__(THREADS) k_histogram(HistParams h)
 
     const size_t gthreads = (size_t)gridDim.x * THREADS;
     const size_t gid = (size_t)blockIdx.x * THREADS + tid;
+    const int lane = tid & 31;
     const T* keys = static_cast<const T*>(h.keys);
+    SkipAcc<KT, !FULLRANGE> acc(keys, h.begin_bit, h.end_bit);
     size_t done = 0;
     if (h.aligned16) {
         const size_t nvec = h.n / VEC;
         const uint4* kv = reinterpret_cast<const uint4*>(keys);
-        size_t v = gid;
-        for (; v + (U - 1) * gthreads < nvec; v += U * gthreads) {
+        // Full rounds (U vectors per thread, the same trip count everywhere),
+        // then what is left.  Thread gid + 1 holds the vector after thread
+        // gid's, so a shuffle brings the next key for the order check.
+        const size_t per_round = U * gthreads, rounds = nvec / per_round;
+        for (size_t r = 0; r < rounds; ++r) {
             uint4 w[U];
+            T nb[U];  // lane 31: the key after its vector, loaded with the round
 #pragma unroll
-            for (int u = 0; u < U; ++u) w[u] = __ldcs(kv + v + u * gthreads);
+            for (int u = 0; u < U; ++u) {
+                const size_t v = r * per_round + u * gthreads + gid;
+                w[u] = __ldcs(kv + v);
+                nb[u] = (lane == 31 && v + 1 < nvec) ? keys[(v + 1) * VEC] : T(0);
+            }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 T k[VEC];
                 memcpy(k, &w[u], 16);
 #pragma unroll
                 for (int j = 0; j < VEC; ++j) count(k[j]);
+                const size_t v = r * per_round + u * gthreads + gid;
+                T first, last;
+                acc.vector(k, first, last);
+                T next = __shfl_down_sync(0xFFFFFFFFu, first, 1);
+                if (lane == 31) next = v + 1 < nvec ? acc.value(nb[u]) : last;
+                acc.pair(last, next);
             }
         }
-        for (; v < nvec; v += gthreads) {
+        for (size_t v = rounds * per_round + gid; v < nvec; v += gthreads) {
             const uint4 w = __ldcs(kv + v);
             T k[VEC];
             memcpy(k, &w, 16);
 #pragma unroll
             for (int j = 0; j < VEC; ++j) count(k[j]);
+            T first, last;
+            acc.vector(k, first, last);
+            if (v + 1 < nvec) acc.pair(last, acc.value(keys[(v + 1) * VEC]));
         }
         done = nvec * VEC;
     }
-    for (size_t i = done + gid; i < h.n; i += gthreads) count(keys[i]);
+    for (size_t i = done + gid; i < h.n; i += gthreads) {
+        const T k = keys[i];
+        count(k);
+        const T v = acc.visit(k);
+        if (i > 0) acc.pair(acc.value(keys[i - 1]), v);
+    }
+    acc.flush_warp(skip_blk);
     __syncthreads();
+    SkipAcc<KT, !FULLRANGE>::template flush_block<RB>(skip_blk, h.skip, h.plan, h.passes, h.begin_bit, h.end_bit);
     for (uint32_t i = tid; i < h.passes * BINS; i += THREADS) {
         uint32_t c = 0;
 #pragma unroll 8
@@ -995,32 +1394,46 @@ rs_status run_passes(Plan& pl)
     uint32_t* alt_vals = reinterpret_cast<uint32_t*>(pl.temp + pl.lay.alt_vals);
     const int P = pl.passes;
 
-    // Destination of pass q: the final pass writes keys_out.
-    auto dst_keys = [&](int q) -> T* { return ((P - 1 - q) % 2 == 0) ? static_cast<T*>(pl.keys_out) : alt_keys; };
-    auto dst_vals = [&](int q) -> uint32_t* { return ((P - 1 - q) % 2 == 0) ? pl.vals_out : alt_vals; };
-
-    const T* src_keys0 = static_cast<const T*>(pl.keys_in);
-    const uint32_t* src_vals0 = pl.vals_in;
-    // In place with an odd number of passes: pass 0 would overwrite keys it
-    // has not read yet, so start from a copy in the ping-pong buffer.
-    const bool copy_first = (pl.keys_in == pl.keys_out) && (P % 2 == 1);
-    if (copy_first) {
-        if (!pl.count_only) {
-            if (cudaMemcpyAsync(alt_keys, pl.keys_in, pl.n * KB, cudaMemcpyDeviceToDevice, pl.stream) != cudaSuccess)
-                return RS_ERR_CUDA;
-            if (VALS && cudaMemcpyAsync(alt_vals, pl.vals_in, pl.n * 4, cudaMemcpyDeviceToDevice, pl.stream) != cudaSuccess)
-                return RS_ERR_CUDA;
-        }
-        src_keys0 = alt_keys;
-        src_vals0 = alt_vals;
-    }
-    // With copy_first, pass 0 (reading alt) writes keys_out because P is odd.
-
+    // The host plans each pass's buffers for the case where every pass runs
+    // (chain_is_out with E = P); a pass kernel that finds some pass skipped
+    // works out its own from the sort-level buffers (pass_buffers).
+    const bool in_place = pl.keys_in == pl.keys_out;
     PassParams base{};
+    base.sort_keys_in = pl.keys_in;
+    base.sort_keys_out = pl.keys_out;
+    base.sort_vals_in = VALS ? pl.vals_in : nullptr;
+    base.sort_vals_out = VALS ? pl.vals_out : nullptr;
+    base.alt_keys = alt_keys;
+    base.alt_vals = VALS ? alt_vals : nullptr;
+    base.skip = meta + kSkipBase;
+    base.plan = meta + kPlanBase;
+    base.passes = (uint32_t)P;
+    base.begin_bit = (uint32_t)pl.begin_bit;
+    base.end_bit = (uint32_t)pl.end_bit;
+    base.in_place = in_place ? 1u : 0u;
     base.n = n;
     base.err = meta + kErrWord;
     base.spin_limit = pl.spin_limit;
     base.stall_tile = pl.stall_tile;
+    const int sms = pl.count_only ? 1 : device_sm_count();
+
+    auto plan_buffers = [&](PassParams& pp, int q) {
+        const uint32_t E = (uint32_t)P, j = (uint32_t)q;
+        const bool src_out = chain_is_out(j, E, in_place), dst_out = chain_is_out(j + 1, E, in_place);
+        pp.keys_in = j == 0 ? pl.keys_in : (src_out ? pl.keys_out : static_cast<const void*>(alt_keys));
+        pp.keys_out = dst_out ? pl.keys_out : static_cast<void*>(alt_keys);
+        if (VALS) {
+            pp.vals_in = j == 0 ? pl.vals_in : (src_out ? pl.vals_out : alt_vals);
+            pp.vals_out = dst_out ? pl.vals_out : alt_vals;
+        }
+    };
+
+    // In place, a final copy (k_chain_copy) runs when an odd number of passes ran.
+    auto finish = [&]() -> rs_status {
+        if (!in_place) return RS_OK;
+        if (!pl.count_only) k_chain_copy<RB, T, VALS><<<4 * sms, 256, 0, pl.stream>>>(base);
+        return after_launch(pl, kKindCopy);
+    };
 
     if (pl.algo == RS_ALGO_ONESWEEP) {
         constexpr int THREADS = tile_threads(kAlgoOnesweep, KB, VALS);
@@ -1030,7 +1443,8 @@ rs_status run_passes(Plan& pl)
         base.num_tiles = num_tiles;
         constexpr int MAXP = (8 * KB + RB - 1) / RB;
         constexpr int HCOLS = (MAXP * (1 << RB) * 32 * 4 <= 160 * 1024) ? 32 : 16;
-        auto hk = k_histogram<KT, RB, 1024, HCOLS>;
+        const bool full_range = pl.begin_bit == 0 && pl.end_bit == 8 * KB;
+        auto hk = full_range ? k_histogram<KT, RB, 1024, HCOLS, true> : k_histogram<KT, RB, 1024, HCOLS, false>;
         auto pk = k_onesweep<KT, RB, THREADS, ITEMS, VALS>;
         auto pkb = k_onesweep<ByteTwin<KT>::value, RB, THREADS, ITEMS, VALS>;
         if (!pl.count_only && (!set_smem(pk, S::bytes) || !set_smem(pkb, S::bytes))) return RS_ERR_CUDA;
@@ -1045,7 +1459,8 @@ rs_status run_passes(Plan& pl)
         h.zero = reinterpret_cast<uint4*>(big);
         h.zero_vec4 = status_words / 4;
         h.aligned16 = (reinterpret_cast<uintptr_t>(pl.keys_in) % 16) == 0;
-        const int sms = pl.count_only ? 1 : device_sm_count();
+        h.skip = meta + kSkipBase;
+        h.plan = meta + kPlanBase;
         const size_t want = (n + 1024 * 16 - 1) / (1024 * 16);
         const int hgrid = (int)std::max<size_t>(1, std::min<size_t>(want, (size_t)sms));
         const size_t hsmem = (size_t)P * BINS * HCOLS * 4;
@@ -1053,20 +1468,10 @@ rs_status run_passes(Plan& pl)
         if (!pl.count_only) hk<<<hgrid, 1024, hsmem, pl.stream>>>(h);
         rs_status st = after_launch(pl, kKindHistogram);
         if (st != RS_OK) return st;
-        uint32_t os_grid = num_tiles;
-        if (!pl.count_only) {
-            int occ = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, pk, THREADS, S::bytes) != cudaSuccess || occ < 1)
-                occ = 1;
-            os_grid = RS_OS_PERSISTENT ? (uint32_t)std::min<size_t>((size_t)sms * occ, num_tiles) : num_tiles;
-            (void)pkb;
-        }
         for (int q = 0; q < P; ++q) {
             PassParams pp = base;
-            pp.keys_in = q == 0 ? (const void*)src_keys0 : (const void*)dst_keys(q - 1);
-            pp.keys_out = dst_keys(q);
-            pp.vals_in = VALS ? (q == 0 ? src_vals0 : dst_vals(q - 1)) : nullptr;
-            pp.vals_out = VALS ? dst_vals(q) : nullptr;
+            pp.pass = (uint32_t)q;
+            plan_buffers(pp, q);
             pp.shift = pl.begin_bit + q * RB;
             const uint32_t width = std::min(RB, pl.end_bit - (int)pp.shift);
             pp.mask = (1u << width) - 1u;
@@ -1074,11 +1479,11 @@ rs_status run_passes(Plan& pl)
             pp.ghist = meta + kGhistBase + q * BINS;
             pp.ticket = meta + kTicketBase + q;
             const bool byte_digit = (RB == 8) && (pp.shift % 8 == 0) && (pp.mask == 0xFFu);
-            if (!pl.count_only) (byte_digit ? pkb : pk)<<<os_grid, THREADS, S::bytes, pl.stream>>>(pp);
+            if (!pl.count_only) (byte_digit ? pkb : pk)<<<num_tiles, THREADS, S::bytes, pl.stream>>>(pp);
             st = after_launch(pl, kKindOnesweep);
             if (st != RS_OK) return st;
         }
-        return RS_OK;
+        return finish();
     }
 
     // Reduce-then-scan.
@@ -1087,7 +1492,8 @@ rs_status run_passes(Plan& pl)
     using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
     const uint32_t num_tiles = (n + TILE - 1) / TILE;
     base.num_tiles = num_tiles;
-    auto uk = k_upsweep<KT, RB, 512, TILE>;
+    auto uk0 = k_upsweep<KT, RB, 512, TILE, true>;
+    auto uk = k_upsweep<KT, RB, 512, TILE, false>;
     auto dk = k_downsweep<KT, RB, THREADS, ITEMS, VALS>;
     auto dkb = k_downsweep<ByteTwin<KT>::value, RB, THREADS, ITEMS, VALS>;
     if (!pl.count_only && (!set_smem(dk, S::bytes) || !set_smem(dkb, S::bytes))) return RS_ERR_CUDA;
@@ -1096,29 +1502,26 @@ rs_status run_passes(Plan& pl)
         int occ = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, dk, THREADS, S::bytes) != cudaSuccess || occ < 1)
             occ = 1;
-        G = (uint32_t)std::min<size_t>((size_t)device_sm_count() * occ, (size_t)kRtsMaxCtas);
+        G = (uint32_t)std::min<size_t>((size_t)sms * occ, (size_t)kRtsMaxCtas);
     }
     G = std::max<uint32_t>(1, std::min<uint32_t>(G, num_tiles));
     const uint32_t tpc = (num_tiles + G - 1) / G;
     G = (num_tiles + tpc - 1) / tpc;
     for (int q = 0; q < P; ++q) {
         PassParams pp = base;
-        pp.keys_in = q == 0 ? (const void*)src_keys0 : (const void*)dst_keys(q - 1);
-        pp.keys_out = dst_keys(q);
-        pp.vals_in = VALS ? (q == 0 ? src_vals0 : dst_vals(q - 1)) : nullptr;
-        pp.vals_out = VALS ? dst_vals(q) : nullptr;
+        pp.pass = (uint32_t)q;
+        plan_buffers(pp, q);
         pp.shift = pl.begin_bit + q * RB;
         const uint32_t width = std::min(RB, pl.end_bit - (int)pp.shift);
         pp.mask = (1u << width) - 1u;
         pp.counts = big;
         pp.G = G;
         pp.tiles_per_cta = tpc;
-        if (!pl.count_only) uk<<<G, 512, 0, pl.stream>>>(pp);
+        if (!pl.count_only) (q == 0 ? uk0 : uk)<<<G, 512, 0, pl.stream>>>(pp);
         rs_status st = after_launch(pl, kKindUpsweep);
         if (st != RS_OK) return st;
         pp.ghist = meta + kGhistBase + q * BINS;  // row totals of this pass
-        if (!pl.count_only)
-            k_spine_scan<256><<<BINS, 256, 0, pl.stream>>>(big, G, meta + kGhistBase + q * BINS);
+        if (!pl.count_only) k_spine_scan<RB, 256><<<BINS, 256, 0, pl.stream>>>(pp, meta + kGhistBase + q * BINS);
         st = after_launch(pl, kKindSpine);
         if (st != RS_OK) return st;
         const bool byte_digit = (RB == 8) && (pp.shift % 8 == 0) && (pp.mask == 0xFFu);
@@ -1126,7 +1529,7 @@ rs_status run_passes(Plan& pl)
         st = after_launch(pl, kKindDownsweep);
         if (st != RS_OK) return st;
     }
-    return RS_OK;
+    return finish();
 }
 
 template <int KT>

@@ -16,9 +16,10 @@ def to_dev(a, dev):
 
 
 def gpu_sort(kt, keys, vals=None, begin_bit=0, end_bit=None, algo="auto", radix_bits=0,
-             dev="cuda:0", offset=0, in_place=False, check_status=True):
+             dev="cuda:0", offset=0, in_place=False, check_status=True, want_record=False):
     """Sort on the GPU via rs_sort; `offset` elements of padding before the
-    input exercise unaligned pointers.  Returns (keys, vals) as numpy."""
+    input exercise unaligned pointers.  Returns (keys, vals) as numpy, plus
+    the pass-skip record (differing_bits, unordered) if want_record."""
     import torch
     end_bit = rs.KEY_BITS[kt] if end_bit is None else end_bit
     n = len(keys)
@@ -48,4 +49,8 @@ def gpu_sort(kt, keys, vals=None, begin_bit=0, end_bit=None, algo="auto", radix_
     ko = kout.cpu().numpy().view(NP_KEY[kt]) if n else np.empty(0, NP_KEY[kt])
     vo = None if vals is None else (vout.cpu().numpy().view(np.uint32) if n else np.empty(0, np.uint32))
     assert kb == ko.dtype.itemsize
+    if want_record:
+        st, bits, unordered = rs.rs_skip_record(temp)
+        assert st == 0
+        return ko, vo, (bits, unordered)
     return ko, vo

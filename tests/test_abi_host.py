@@ -70,6 +70,13 @@ def test_kernel_counts(lib):
     assert count("u32", 1 << 26, 0, 32, "auto", vals=True) == 12
     assert count("u64", 1 << 26, 0, 64, "auto") == 24
     assert count("u32", 1 << 30, 0, 32, "auto") == 12
+    # In place: one more kernel, the copy back from temp after an odd number
+    # of running passes (it returns at once otherwise).
+    fake = 1 << 40
+    inplace = rs.make_desc("u32", fake, fake, None, None, 1 << 20, 0, 32, None, 0, 0, "onesweep")
+    assert rs.rs_sort_kernel_count(inplace) == 1 + 4 + 1
+    inplace = rs.make_desc("u32", fake, fake, None, None, 1 << 26, 0, 24, None, 0, 0, "reduce_scan")
+    assert rs.rs_sort_kernel_count(inplace) == 3 * 3 + 1
 
 
 FAKE = 1 << 40  # 256-byte aligned addresses that are never dereferenced
