@@ -36,7 +36,7 @@ DEFAULT_WORKLOAD = "c4a_u32_2p28"
 L2_BYTES = 126 * 2**20
 FALLBACK_HBM_GBS = 6800.0
 KIND_NAMES = {1: "histogram", 2: "onesweep_pass", 3: "upsweep", 4: "spine_scan", 5: "downsweep",
-              6: "copy"}
+              6: "copy", 7: "cluster_sort"}
 
 
 def parse():
@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--log2n", type=int, default=None, help="override the size (uniform u32 sweep)")
-    ap.add_argument("--algo", default="auto", choices=["auto", "onesweep", "reduce_scan"])
+    ap.add_argument("--algo", default="auto", choices=["auto", "onesweep", "reduce_scan", "cluster"])
     ap.add_argument("--radix-bits", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -314,7 +314,8 @@ def run_ours(args):
     passes = -(-(e - b) // (args.radix_bits or 8)) if e > b else 0
     # algorithmic bytes per launch of each kernel kind
     algo_bytes = {1: n * kbytes, 2: n * 2 * (kbytes + vbytes), 3: n * kbytes, 4: 0,
-                  5: n * (kbytes + 2 * (kbytes + vbytes)) - n * kbytes}
+                  5: n * (kbytes + 2 * (kbytes + vbytes)) - n * kbytes, 6: n * 2 * (kbytes + vbytes),
+                  7: n * 2 * (kbytes + vbytes)}
     dominant = max(per_kind, key=lambda k: sum(per_kind[k]))
     dom_ms = statistics.mean(per_kind[dominant])
     dom_bytes = algo_bytes[dominant]
@@ -323,9 +324,12 @@ def run_ours(args):
                                "avg_ms": round(statistics.mean(v), 4),
                                "share": round(sum(v) / sum(sum(x) for x in per_kind.values()), 4)}
                for k, v in per_kind.items()}
-    resolved = "onesweep" if 2 in per_kind else "reduce_scan"
-    scheme_bpk = ((kbytes if resolved == "onesweep" else passes * kbytes)
-                  + passes * 2 * (kbytes + vbytes))
+    resolved = "cluster" if 7 in per_kind else "onesweep" if 2 in per_kind else "reduce_scan"
+    if resolved == "cluster":  # global memory is read once and written once
+        scheme_bpk = 2 * (kbytes + vbytes)
+    else:
+        scheme_bpk = ((kbytes if resolved == "onesweep" else passes * kbytes)
+                      + passes * 2 * (kbytes + vbytes))
     ideal_bpk = passes * 2 * (kbytes + vbytes)
     sort_gbs = n * scheme_bpk / (ms_per_step * 1e-3) / 1e9
 

@@ -87,10 +87,15 @@ typedef enum rs_status {
 typedef enum rs_key_type { RS_U32 = 0, RS_I32 = 1, RS_F32 = 2, RS_U64 = 3 } rs_key_type;
 
 typedef enum rs_algo {
-    RS_ALGO_AUTO = 0,        /* reduce-then-scan for n >= 2^25, the chained scan
-                                below (both measured on GB300)                   */
+    RS_ALGO_AUTO = 0,        /* the cluster sort for n <= rs_cluster_max_n(),
+                                reduce-then-scan for n >= 2^25, the chained scan
+                                between (measured on GB300)                      */
     RS_ALGO_ONESWEEP = 1,    /* one upfront histogram read + one kernel per pass    */
-    RS_ALGO_REDUCE_SCAN = 2  /* upsweep + spine scan + downsweep per pass           */
+    RS_ALGO_REDUCE_SCAN = 2, /* upsweep + spine scan + downsweep per pass           */
+    RS_ALGO_CLUSTER = 3      /* the whole sort in ONE kernel on a thread-block
+                                cluster, keys held in distributed shared memory
+                                between passes; n <= rs_cluster_max_n(), else
+                                RS_ERR_UNSUPPORTED                               */
 } rs_algo;
 
 /*
@@ -162,11 +167,21 @@ rs_status rs_sort(const rs_sort_desc* desc);
  * return *num_kernels is the number of kernels launched and kinds[i] (if
  * kinds != NULL, max_events entries) names kernel i+1's role:
  *   1 histogram (all passes), 2 chained-scan pass, 3 upsweep, 4 spine scan,
- *   5 downsweep, 6 copy.
+ *   5 downsweep, 6 copy, 7 cluster sort (the whole sort).
  * Returns RS_ERR_INVALID_ARG if max_events is smaller than kernels + 1.
  */
 rs_status rs_sort_profiled(const rs_sort_desc* desc, void* const* events, int max_events,
                            int* num_kernels, int* kinds);
+
+/*
+ * Largest n the cluster schedule (RS_ALGO_CLUSTER) sorts: 16 CTAs x one tile
+ * each -- 65536 uint32/int32/float keys, 49152 of them with values or uint64
+ * keys, 32768 uint64 keys with values.  Up to half of that runs on 8 CTAs
+ * (the portable cluster size); above it the cluster needs 16, which a device
+ * may not schedule: then RS_ALGO_CLUSTER returns RS_ERR_UNSUPPORTED and AUTO
+ * takes the chained scan.  No CUDA call; 0 for an invalid key type.
+ */
+size_t rs_cluster_max_n(rs_key_type key_type, int with_values);
 
 /*
  * Number of kernels rs_sort would launch for this descriptor (no launch).

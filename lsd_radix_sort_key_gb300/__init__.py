@@ -20,12 +20,12 @@ from . import _build
 KEY_TYPES = {"u32": 0, "i32": 1, "f32": 2, "u64": 3}
 KEY_BYTES = {"u32": 4, "i32": 4, "f32": 4, "u64": 8}
 KEY_BITS = {"u32": 32, "i32": 32, "f32": 32, "u64": 64}
-ALGOS = {"auto": 0, "onesweep": 1, "reduce_scan": 2}
+ALGOS = {"auto": 0, "onesweep": 1, "reduce_scan": 2, "cluster": 3}
 STATUS = {0: "RS_OK", 1: "RS_ERR_INVALID_ARG", 2: "RS_ERR_TEMP_TOO_SMALL", 3: "RS_ERR_ALIAS",
           4: "RS_ERR_CUDA", 5: "RS_ERR_DEVICE_TIMEOUT", 6: "RS_ERR_CHECK_FAILED",
           7: "RS_ERR_UNSUPPORTED"}
 KERNEL_KINDS = {1: "histogram", 2: "onesweep_pass", 3: "upsweep", 4: "spine_scan",
-                5: "downsweep", 6: "copy"}
+                5: "downsweep", 6: "copy", 7: "cluster_sort"}
 LIB_PATH = _build.LIB
 
 
@@ -60,6 +60,7 @@ SIGNATURES = {
     "rs_sort_kernel_count": (_i, [ctypes.POINTER(SortDesc)]),
     "rs_device_status": (_i, [_vp, _vp]),
     "rs_skip_record": (_i, [_vp, _vp, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(_i)]),
+    "rs_cluster_max_n": (_sz, [_i, _i]),
     "rs_status_string": (ctypes.c_char_p, [_i]),
     "rs_graph_create": (_i, [ctypes.POINTER(SortDesc), ctypes.POINTER(_vp)]),
     "rs_graph_launch": (_i, [_vp, _vp]),
@@ -190,6 +191,11 @@ def rs_sort_profiled(desc: SortDesc, events):
 
 def rs_device_status(temp, stream=None) -> int:
     return lib().rs_device_status(_addr(temp), _stream(stream))
+
+
+def rs_cluster_max_n(key_type: str, with_values: bool) -> int:
+    """Largest n the one-kernel cluster schedule sorts."""
+    return lib().rs_cluster_max_n(KEY_TYPES[key_type], int(bool(with_values)))
 
 
 def rs_skip_record(temp, stream=None):

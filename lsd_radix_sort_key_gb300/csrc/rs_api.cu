@@ -54,7 +54,8 @@ rs_status make_plan(const rs_sort_desc* d, rs::Plan* pl)
     const bool vals = d->vals_in != nullptr || d->vals_out != nullptr;
     if (vals && (!d->vals_in || !d->vals_out)) return RS_ERR_INVALID_ARG;
     if (d->radix_bits != 0 && d->radix_bits != 4 && d->radix_bits != 8) return RS_ERR_INVALID_ARG;
-    if (d->algo != RS_ALGO_AUTO && d->algo != RS_ALGO_ONESWEEP && d->algo != RS_ALGO_REDUCE_SCAN)
+    if (d->algo != RS_ALGO_AUTO && d->algo != RS_ALGO_ONESWEEP && d->algo != RS_ALGO_REDUCE_SCAN &&
+        d->algo != RS_ALGO_CLUSTER)
         return RS_ERR_INVALID_ARG;
     if (d->stall_tile < 0) return RS_ERR_INVALID_ARG;
     const size_t n = d->n;
@@ -68,14 +69,18 @@ rs_status make_plan(const rs_sort_desc* d, rs::Plan* pl)
     pl->radix_bits = d->radix_bits == 0 ? 8 : d->radix_bits;
     pl->passes = rs::passes_for(d->begin_bit, d->end_bit, pl->radix_bits);
     pl->algo = d->algo;
+    const size_t cluster_max = rs::cluster_max_n(kb, vals);
     if (pl->algo == RS_ALGO_AUTO) {
-        // Chosen by measurement on GB300: reduce-then-scan is faster from 2^25
-        // keys for every key type, with or without values; the chained scan
-        // (fewer launches) below that.  The chained scan needs n < 2^30.
+        // Chosen by measurement on GB300: one cluster kernel while the keys fit
+        // in 8 CTAs' shared memory; reduce-then-scan from 2^25 keys for every
+        // key type, with or without values; the chained scan (fewer launches)
+        // between.  The chained scan needs n < 2^30.
         const bool rts = n > kOnesweepMaxN || n >= kAutoReduceScanMinN;
-        pl->algo = rts ? RS_ALGO_REDUCE_SCAN : RS_ALGO_ONESWEEP;
+        pl->algo = n <= cluster_max ? RS_ALGO_CLUSTER : rts ? RS_ALGO_REDUCE_SCAN : RS_ALGO_ONESWEEP;
+        pl->auto_chosen = true;
     }
     if (pl->algo == RS_ALGO_ONESWEEP && n > kOnesweepMaxN) return RS_ERR_UNSUPPORTED;
+    if (pl->algo == RS_ALGO_CLUSTER && n > cluster_max) return RS_ERR_UNSUPPORTED;
     pl->keys_in = d->keys_in;
     pl->keys_out = d->keys_out;
     pl->vals_in = d->vals_in;
@@ -257,6 +262,12 @@ rs_status rs_device_status(const void* temp, void* stream)
     if (word & (1u << RS_ERR_DEVICE_TIMEOUT)) return RS_ERR_DEVICE_TIMEOUT;
     if (word) return RS_ERR_CHECK_FAILED;
     return RS_OK;
+}
+
+size_t rs_cluster_max_n(rs_key_type key_type, int with_values)
+{
+    if (!valid_kt(key_type)) return 0;
+    return rs::cluster_max_n(key_bytes(key_type), with_values != 0);
 }
 
 rs_status rs_skip_record(const void* temp, void* stream, uint64_t* differing_bits, int* unordered)

@@ -73,6 +73,40 @@ constexpr int tile_keys(int algo, int key_bytes, bool vals)
     return tile_threads(algo, key_bytes, vals) * tile_items(key_bytes, vals);
 }
 
+// Small sorts: one kernel on a cluster of at most kClusterMaxCtas CTAs, each
+// holding one tile of kClusterThreads x cluster_items keys in shared memory.
+// 16 CTAs of 512 x 8 measured fastest on GB300 for 2^12..2^16 uint32 keys
+// (8 CTAs of 512 x 16: 1.3x slower; 16 of 1024 x 4 or 256 x 16: 1.07x).
+// 16 is above the portable cluster size: the launch opts in, and a device
+// that cannot schedule it falls back to the chained scan (AUTO).
+#ifndef RS_CL_MAX_CTAS
+#define RS_CL_MAX_CTAS 16
+#endif
+#ifndef RS_CL_THREADS
+#define RS_CL_THREADS 512
+#endif
+#ifndef RS_CL_ITEMS
+#define RS_CL_ITEMS 8
+#endif
+constexpr int kClusterMaxCtas = RS_CL_MAX_CTAS;
+constexpr int kClusterThreads = RS_CL_THREADS;
+constexpr int cluster_items(int key_bytes, bool vals)
+{
+    // uint32 keys RS_CL_ITEMS per thread; 3/4 of that with values or for
+    // uint64 keys, 9/16 for uint64 keys with values (registers and shared
+    // memory scale with the bytes per key)
+    return key_bytes == 4 ? (vals ? RS_CL_ITEMS * 3 / 4 : RS_CL_ITEMS)
+                          : (vals ? RS_CL_ITEMS * 9 / 16 : RS_CL_ITEMS * 3 / 4);
+}
+constexpr size_t cluster_tile_keys(int key_bytes, bool vals)
+{
+    return (size_t)kClusterThreads * cluster_items(key_bytes, vals);
+}
+constexpr size_t cluster_max_n(int key_bytes, bool vals)
+{
+    return (size_t)kClusterMaxCtas * cluster_tile_keys(key_bytes, vals);
+}
+
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 constexpr int passes_for(int begin_bit, int end_bit, int radix_bits)

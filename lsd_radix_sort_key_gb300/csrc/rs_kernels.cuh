@@ -38,6 +38,7 @@
 // is needed and NaN/Inf payloads come back unchanged.
 #pragma once
 
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -1194,6 +1195,215 @@ __global__ void __launch_bounds__(256) k_chain_copy(PassParams p)
                        (size_t)gridDim.x * blockDim.x);
 }
 
+// ------------------------------------------------------------ small sorts
+//
+// A sort of at most kClusterMaxCtas tiles runs as ONE kernel on a thread-block
+// cluster: CTA c holds positions [c*TILE, (c+1)*TILE) of the current order in
+// its shared memory, for every pass.  A pass ranks and shuffles the CTA's tile
+// exactly as a chained-scan tile does; the CTAs then exchange their digit
+// counts through distributed shared memory -- the start of digit d in CTA c
+// is every CTA's count of smaller digits plus CTA 0..c-1's count of d, the
+// digit-major exclusive scan ("Radix sort paralelo sobre el scan", section
+// "Las tres fases de una pasada") over C blocks -- and every key is stored
+// straight into the shared memory of the CTA that owns its new position (the
+// last running pass writes keys_out).  Two cluster barriers per pass; global
+// memory is read once and written once.
+
+struct ClusterParams {
+    const void* keys_in;
+    void* keys_out;
+    const uint32_t* vals_in;
+    uint32_t* vals_out;
+    uint32_t n;
+    uint32_t passes;
+    uint32_t begin_bit;
+    uint32_t end_bit;
+    uint32_t* err;
+    uint32_t* skip;   // the skip record, for rs_skip_record
+};
+
+template <typename T, int RB, int THREADS, int ITEMS, bool VALS>
+struct ClusterSmem {
+    using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
+    static constexpr size_t next_keys_off = align_up(S::bytes, 16);  // this CTA's keys of the next pass
+    static constexpr size_t next_vals_off = next_keys_off + align_up(sizeof(T) * S::TILE, 16);
+    static constexpr size_t cnt_off = next_vals_off + (VALS ? align_up(4 * (size_t)S::TILE, 16) : 0);
+    static constexpr size_t rec_off = cnt_off + 4 * S::BINS;  // this CTA's share of the skip record
+    static constexpr size_t plan_off = rec_off + 16;          // run mask, running passes
+    static constexpr size_t bytes = plan_off + 16;
+};
+
+template <int KT, int RB, int THREADS, int ITEMS, bool VALS>
+__global__ void __launch_bounds__(THREADS, 1) k_cluster_sort(ClusterParams cp)
+{
+    namespace cg = cooperative_groups;
+    using T = typename KeyOps<KT>::T;
+    using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
+    using CS = ClusterSmem<T, RB, THREADS, ITEMS, VALS>;
+    constexpr int BINS = S::BINS;
+    constexpr uint32_t M = S::TILE;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const T* skeys = reinterpret_cast<const T*>(smem + S::keys_off);
+    const uint32_t* svals = reinterpret_cast<const uint32_t*>(smem + S::vals_off);
+    uint32_t* sbase = reinterpret_cast<uint32_t*>(smem + S::base_off);
+    uint32_t* sscan = reinterpret_cast<uint32_t*>(smem + S::scan_off);
+    T* nkeys = reinterpret_cast<T*>(smem + CS::next_keys_off);
+    uint32_t* nvals = reinterpret_cast<uint32_t*>(smem + CS::next_vals_off);
+    uint32_t* cnts = reinterpret_cast<uint32_t*>(smem + CS::cnt_off);
+    uint32_t* rec = reinterpret_cast<uint32_t*>(smem + CS::rec_off);
+    uint32_t* plan = reinterpret_cast<uint32_t*>(smem + CS::plan_off);
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const uint32_t c = cluster.block_rank(), C = cluster.num_blocks();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t lo = c * M;
+    const uint32_t valid = cp.n > lo ? min(cp.n - lo, M) : 0u;
+    const uint32_t seg = (uint32_t)warp * (32u * ITEMS);
+    const T* gin = static_cast<const T*>(cp.keys_in);
+    PassParams p{};
+    p.n = valid;  // the tile code guards positions against its tile's key count
+    p.err = cp.err;
+
+    // 1. This CTA's keys, warp-striped (as load_tile), from global memory.
+    T key[ITEMS];
+    uint32_t val[VALS ? ITEMS : 1];
+    if (valid == M) {
+        load_striped<true, T, ITEMS>(gin + lo, seg, valid, lane, key);
+        if constexpr (VALS) load_striped<true, uint32_t, ITEMS>(cp.vals_in + lo, seg, valid, lane, val);
+    } else {
+        load_striped<false, T, ITEMS>(gin + lo, seg, valid, lane, key);
+        if constexpr (VALS) load_striped<false, uint32_t, ITEMS>(cp.vals_in + lo, seg, valid, lane, val);
+    }
+
+    // 2. The skip record: each CTA's share of diff and of the order check
+    // (pairs inside the tile from registers, across warps and CTAs from
+    // global memory), then every CTA combines all shares into the same plan.
+    if (tid < 4) rec[tid] = 0u;
+    __syncthreads();
+    {
+        SkipAcc<KT> acc(gin, cp.begin_bit, cp.end_bit);
+        T v[ITEMS];
+#pragma unroll
+        for (int k = 0; k < ITEMS; ++k) {
+            const uint32_t pos = seg + k * 32 + lane;
+            v[k] = pos < valid ? acc.visit(key[k]) : T(0);
+        }
+#pragma unroll
+        for (int k = 0; k < ITEMS; ++k) {
+            const uint32_t pos = seg + k * 32 + lane;
+            T nx = __shfl_down_sync(0xFFFFFFFFu, v[k], 1);
+            if (k + 1 < ITEMS) {
+                const T first_next = __shfl_sync(0xFFFFFFFFu, v[k + 1 < ITEMS ? k + 1 : k], 0);
+                if (lane == 31) nx = first_next;
+            } else if (lane == 31 && pos + 1 < valid) {
+                nx = acc.value(gin[lo + pos + 1]);
+            }
+            if (pos + 1 < valid) acc.pair(v[k], nx);
+        }
+        if (tid == 0 && lo > 0 && valid > 0) acc.pair(acc.value(gin[lo - 1]), acc.value(gin[lo]));
+        acc.flush_warp(rec);
+    }
+    __syncthreads();
+    cluster.sync();  // every CTA's share is complete
+    if (tid == 0) {
+        uint32_t d_lo = 0, d_hi = 0, un = 0;
+        for (uint32_t r = 0; r < C; ++r) {
+            const uint32_t* rr = cluster.map_shared_rank(rec, r);
+            d_lo |= rr[0];
+            d_hi |= rr[1];
+            un |= rr[2];
+        }
+        uint32_t words[kMaxPasses];
+        write_plan<RB>(d_lo, d_hi, un, words, cp.passes, cp.begin_bit, cp.end_bit);
+        uint32_t mask = 0;
+        for (uint32_t q = 0; q < cp.passes; ++q) mask |= (words[q] & 1u) << q;
+        plan[0] = mask;
+        plan[1] = cp.passes ? (words[0] >> 16) & 0xFFu : 0u;
+        if (c == 0) {
+            cp.skip[0] = d_lo;
+            cp.skip[1] = d_hi;
+            cp.skip[2] = un ? 1u : 0u;
+        }
+    }
+    __syncthreads();
+    const uint32_t run_mask = plan[0], E = plan[1];
+    // A CTA's shared memory must not be read after it exits: with no pass to
+    // run, wait here until every CTA has read the others' shares (otherwise
+    // the first pass's barrier does).
+    if (E == 0u) cluster.sync();
+
+    // 3. The running passes.
+    uint32_t j = 0;
+    for (uint32_t q = 0; q < cp.passes; ++q) {
+        if (!((run_mask >> q) & 1u)) continue;
+        if (j > 0) {  // this CTA's keys of this pass, left by the previous one
+            if (valid == M) {
+                load_striped<true, T, ITEMS>(nkeys, seg, valid, lane, key);
+                if constexpr (VALS) load_striped<true, uint32_t, ITEMS>(nvals, seg, valid, lane, val);
+            } else {
+                load_striped<false, T, ITEMS>(nkeys, seg, valid, lane, key);
+                if constexpr (VALS) load_striped<false, uint32_t, ITEMS>(nvals, seg, valid, lane, val);
+            }
+        }
+        p.shift = cp.begin_bit + q * RB;
+        p.mask = (1u << min((uint32_t)RB, cp.end_bit - p.shift)) - 1u;
+        zero_counters<S>(smem, THREADS);
+        __syncthreads();
+        uint32_t cnt, start;
+        if (valid == M)
+            tile_rank_and_shuffle<true, KT, RB, THREADS, ITEMS, VALS>(p, smem, 0, key, val, &cnt, &start,
+                                                                      [](int, uint32_t) {});
+        else
+            tile_rank_and_shuffle<false, KT, RB, THREADS, ITEMS, VALS>(p, smem, 0, key, val, &cnt, &start,
+                                                                       [](int, uint32_t) {});
+        if (tid < BINS) cnts[tid] = cnt;
+        // Counts published; every CTA has also read its keys of this pass, so
+        // the next-pass buffers may be written from here on.
+        cluster.sync();
+        uint32_t tot = 0, before = 0;
+        if (tid < BINS) {
+            for (uint32_t r = 0; r < C; ++r) {
+                const uint32_t x = *cluster.map_shared_rank(cnts + tid, r);
+                tot += x;
+                before += r < c ? x : 0u;
+            }
+        }
+        const uint32_t dstart = bins_exclusive_scan<BINS>(tid < BINS ? tot : 0u, sscan, nullptr);
+        if (tid < BINS) sbase[tid] = dstart + before - start;
+        __syncthreads();
+        const bool last = j + 1 == E;
+        T* gout = static_cast<T*>(cp.keys_out);
+        uint32_t bad = 0;
+#pragma unroll
+        for (int k = 0; k < ITEMS; ++k) {
+            const uint32_t s = (uint32_t)(k * THREADS) + tid;
+            if (s < valid) {
+                const T kk = skeys[s];
+                const uint32_t g = sbase[digit_of<KT>(kk, p.shift, p.mask)] + s;
+                if (g >= cp.n) {
+                    bad = 1;
+                    continue;
+                }
+                if (last) {
+                    gout[g] = kk;
+                    if constexpr (VALS) cp.vals_out[g] = svals[s];
+                } else {
+                    const uint32_t dst = g / M, off = g - dst * M;
+                    *cluster.map_shared_rank(nkeys + off, dst) = kk;
+                    if constexpr (VALS) *cluster.map_shared_rank(nvals + off, dst) = svals[s];
+                }
+            }
+        }
+        if (bad) record_error(cp.err, RS_ERR_CHECK_FAILED);
+        cluster.sync();  // the next pass's keys are in place; cnts may be reused
+        ++j;
+    }
+    // No pass runs: the input is the result.
+    if (E == 0u && cp.keys_in != cp.keys_out)
+        copy_span<T, VALS>(gin, static_cast<T*>(cp.keys_out), cp.vals_in, cp.vals_out, lo, lo + valid, tid,
+                           THREADS);
+}
+
 // Chained scan, the one upfront read: the digit histograms of ALL passes,
 // accumulated in shared memory and added to the global ones; the same kernel
 // zeroes the look-back status words of every pass.
@@ -1335,10 +1545,11 @@ struct Plan {
     int launched;
     int* kinds;
     bool count_only;   // only count kernels, launch nothing
+    bool auto_chosen;  // the schedule came from RS_ALGO_AUTO
 };
 
 enum KernelKind { kKindHistogram = 1, kKindOnesweep = 2, kKindUpsweep = 3, kKindSpine = 4,
-                  kKindDownsweep = 5, kKindCopy = 6 };
+                  kKindDownsweep = 5, kKindCopy = 6, kKindCluster = 7 };
 
 // After every launch: check it, and record the next profiling event.
 inline rs_status after_launch(Plan& pl, int kind)
@@ -1532,9 +1743,115 @@ rs_status run_passes(Plan& pl)
     return finish();
 }
 
+// The largest cluster of k_cluster_sort<...> the current device schedules
+// (queried once per device; kClusterMaxCtas when no device is visible, as
+// when only counting kernels on a machine without a GPU).
+template <typename K>
+inline unsigned max_cluster_ctas(K kernel, int threads, size_t smem_bytes)
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return kClusterMaxCtas;
+    }
+    if (cache[dev] == 0) {
+        int size = 0;
+        if (!set_smem(kernel, smem_bytes) ||
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+            cudaGetLastError();
+            size = 1;
+        } else {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(kClusterMaxCtas, 1, 1);
+            cfg.blockDim = dim3(threads, 1, 1);
+            cfg.dynamicSmemBytes = smem_bytes;
+            if (cudaOccupancyMaxPotentialClusterSize(&size, kernel, &cfg) != cudaSuccess || size < 1) {
+                cudaGetLastError();
+                size = 1;
+            }
+        }
+        cache[dev] = std::min(size, kClusterMaxCtas);
+    }
+    return (unsigned)cache[dev];
+}
+
+// CTAs the cluster sort of n keys needs, or 0 if this device cannot run it.
+template <int KT, int RB, bool VALS>
+unsigned cluster_ctas_for(size_t n)
+{
+    using T = typename KeyOps<KT>::T;
+    constexpr int KB = sizeof(T);
+    constexpr int ITEMS = cluster_items(KB, VALS);
+    using CS = ClusterSmem<T, RB, kClusterThreads, ITEMS, VALS>;
+    const size_t tile = cluster_tile_keys(KB, VALS);
+    const size_t ctas = (n + tile - 1) / tile;
+    if (ctas < 1 || ctas > (size_t)kClusterMaxCtas) return 0;
+    if (ctas <= 8) return (unsigned)ctas;  // the portable size always schedules
+    const unsigned cap = max_cluster_ctas(k_cluster_sort<KT, RB, kClusterThreads, ITEMS, VALS>,
+                                          kClusterThreads, CS::bytes);
+    return ctas <= cap ? (unsigned)ctas : 0u;
+}
+
+// The whole sort as one launch on a cluster of ceil(n / tile) CTAs.
+template <int KT, int RB, bool VALS>
+rs_status run_cluster(Plan& pl)
+{
+    using T = typename KeyOps<KT>::T;
+    constexpr int KB = sizeof(T);
+    constexpr int ITEMS = cluster_items(KB, VALS);
+    constexpr int THREADS = kClusterThreads;
+    using CS = ClusterSmem<T, RB, THREADS, ITEMS, VALS>;
+    const unsigned ctas = cluster_ctas_for<KT, RB, VALS>(pl.n);
+    if (ctas == 0) return RS_ERR_UNSUPPORTED;
+    if (pl.count_only) return after_launch(pl, kKindCluster);
+    auto kernel = k_cluster_sort<KT, RB, THREADS, ITEMS, VALS>;
+    if (!set_smem(kernel, CS::bytes)) return RS_ERR_CUDA;
+    if (ctas > 8 && cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        return RS_ERR_CUDA;
+    uint32_t* meta = reinterpret_cast<uint32_t*>(pl.temp + pl.lay.meta);
+    ClusterParams cp{};
+    cp.keys_in = pl.keys_in;
+    cp.keys_out = pl.keys_out;
+    cp.vals_in = VALS ? pl.vals_in : nullptr;
+    cp.vals_out = VALS ? pl.vals_out : nullptr;
+    cp.n = (uint32_t)pl.n;
+    cp.passes = (uint32_t)pl.passes;
+    cp.begin_bit = (uint32_t)pl.begin_bit;
+    cp.end_bit = (uint32_t)pl.end_bit;
+    cp.err = meta + kErrWord;
+    cp.skip = meta + kSkipBase;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = CS::bytes;
+    cfg.stream = pl.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ctas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, cp) != cudaSuccess) return RS_ERR_CUDA;
+    return after_launch(pl, kKindCluster);
+}
+
 template <int KT>
 rs_status run_sort(Plan& pl)
 {
+    if (pl.algo == RS_ALGO_CLUSTER) {
+        const unsigned ctas = pl.vals ? (pl.radix_bits == 4 ? cluster_ctas_for<KT, 4, true>(pl.n)
+                                                            : cluster_ctas_for<KT, 8, true>(pl.n))
+                                      : (pl.radix_bits == 4 ? cluster_ctas_for<KT, 4, false>(pl.n)
+                                                            : cluster_ctas_for<KT, 8, false>(pl.n));
+        if (ctas == 0 && pl.auto_chosen) {
+            pl.algo = RS_ALGO_ONESWEEP;  // this device cannot schedule the cluster
+        } else {
+            if (pl.vals) return pl.radix_bits == 4 ? run_cluster<KT, 4, true>(pl) : run_cluster<KT, 8, true>(pl);
+            return pl.radix_bits == 4 ? run_cluster<KT, 4, false>(pl) : run_cluster<KT, 8, false>(pl);
+        }
+    }
     if (pl.vals) {
         if (pl.radix_bits == 4) return run_passes<KT, 4, true>(pl);
         return run_passes<KT, 8, true>(pl);

@@ -70,6 +70,11 @@ def test_kernel_counts(lib):
     assert count("u32", 1 << 26, 0, 32, "auto", vals=True) == 12
     assert count("u64", 1 << 26, 0, 64, "auto") == 24
     assert count("u32", 1 << 30, 0, 32, "auto") == 12
+    # The cluster schedule: one kernel up to its capacity, refused above it.
+    assert count("u32", 1 << 16, 0, 32, "auto") == 1
+    assert count("u32", 1000, 0, 32, "cluster") == 1
+    assert count("u32", (1 << 16) + 1, 0, 32, "cluster") == -1
+    assert count("u32", (1 << 16) + 1, 0, 32, "auto") == 1 + 4
     # In place: one more kernel, the copy back from temp after an odd number
     # of running passes (it returns at once otherwise).
     fake = 1 << 40
@@ -110,6 +115,7 @@ def desc(**kw):
     (dict(keys_out=FAKE + 4 * 500), 3),               # partial overlap
     (dict(temp=FAKE + 256), 3),                       # temp overlaps the input
     (dict(n=1 << 31, algo="onesweep"), 7),            # chained scan limited to n < 2^30
+    (dict(n=(1 << 16) + 1, algo="cluster"), 7),       # cluster sort limited to its capacity
 ])
 def test_argument_errors(lib, kw, code):
     d = desc(**kw)
@@ -126,6 +132,15 @@ def test_typed_entry_points_validate(lib):
     assert rs.rs_sort_keys_u32(FAKE, 2 * FAKE, 100, 0, 40, 3 * FAKE, 1 << 30, 0) == 1
     assert rs.rs_sort_pairs_f32(FAKE, 2 * FAKE, None, 4 * FAKE, 100, 0, 32, 3 * FAKE, 1 << 30, 0) == 1
     assert rs.rs_sort_keys_u64(FAKE, 2 * FAKE, 100, 0, 64, 3 * FAKE, 10, 0) == 2
+
+
+def test_cluster_capacity(lib):
+    # 16 CTAs x one 512-thread tile: 8 uint32 keys per thread, 6 with values
+    # or for uint64 keys, 4 for uint64 keys with values.
+    assert rs.rs_cluster_max_n("u32", False) == 16 * 512 * 8
+    assert rs.rs_cluster_max_n("f32", True) == 16 * 512 * 6
+    assert rs.rs_cluster_max_n("u64", False) == 16 * 512 * 6
+    assert rs.rs_cluster_max_n("u64", True) == 16 * 512 * 4
 
 
 def test_status_strings(lib):
