@@ -169,6 +169,9 @@ rs_status rs_sort(const rs_sort_desc* desc);
  *   1 histogram (all passes), 2 chained-scan pass, 3 upsweep, 4 spine scan,
  *   5 downsweep, 6 copy, 7 cluster sort (the whole sort).
  * Returns RS_ERR_INVALID_ARG if max_events is smaller than kernels + 1.
+ * While desc->stream is being captured into a CUDA graph the events are
+ * recorded as external event nodes, so every replay of the graph records
+ * them (per-kernel timing of a replayed graph).
  */
 rs_status rs_sort_profiled(const rs_sort_desc* desc, void* const* events, int max_events,
                            int* num_kernels, int* kinds);

@@ -201,7 +201,12 @@ rs_status rs_sort_profiled(const rs_sort_desc* desc, void* const* events, int ma
     pl.events = reinterpret_cast<cudaEvent_t const*>(events);
     pl.max_events = max_events;
     pl.kinds = kinds;
-    if (cudaEventRecord(pl.events[0], pl.stream) != cudaSuccess) return RS_ERR_CUDA;
+    // Inside a stream capture a plain event record only orders the capture;
+    // an external record becomes a graph node that records at every replay.
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(pl.stream, &cs) != cudaSuccess) return RS_ERR_CUDA;
+    pl.event_flags = cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+    if (cudaEventRecordWithFlags(pl.events[0], pl.stream, pl.event_flags) != cudaSuccess) return RS_ERR_CUDA;
     st = enqueue(pl);
     *num_kernels = pl.launched;
     return st;

@@ -1541,6 +1541,7 @@ struct Plan {
     int32_t stall_tile;
     // profiling (optional)
     cudaEvent_t const* events;
+    unsigned event_flags;  // cudaEventRecordExternal while the stream is being captured
     int max_events;
     int launched;
     int* kinds;
@@ -1559,7 +1560,8 @@ inline rs_status after_launch(Plan& pl, int kind)
     if (pl.kinds && pl.launched < pl.max_events) pl.kinds[pl.launched] = kind;
     pl.launched++;
     if (pl.events && pl.launched < pl.max_events)
-        if (cudaEventRecord(pl.events[pl.launched], pl.stream) != cudaSuccess) return RS_ERR_CUDA;
+        if (cudaEventRecordWithFlags(pl.events[pl.launched], pl.stream, pl.event_flags) != cudaSuccess)
+            return RS_ERR_CUDA;
     return RS_OK;
 }
 

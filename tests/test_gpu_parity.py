@@ -209,6 +209,38 @@ def test_profiled_entry_point():
     assert np.array_equal(kout.cpu().numpy().view(np.uint32), oracle.sort("u32", keys)[0])
 
 
+def test_profiled_sorts_captured_in_a_graph():
+    # Under stream capture the events become graph nodes: every replay records
+    # them, and the sorts inside the graph are still correct.
+    dev = "cuda:0"
+    n = 1 << 20
+    keys = synth.u32_uniform(n, 51)
+    kin = to_dev(keys, dev)
+    kout = torch.empty_like(kin)
+    tb = rs.rs_temp_bytes("u32", False, n, 0, 32)
+    temp = torch.empty(tb, dtype=torch.uint8, device=dev)
+    cap = torch.cuda.Stream()
+    d = rs.make_desc("u32", kin, kout, None, None, n, 0, 32, temp, tb, cap, "reduce_scan")
+    steps = [[torch.cuda.Event(enable_timing=True) for _ in range(14)] for _ in range(3)]
+    for ev in steps:  # a plain run first: library caches filled outside the capture
+        assert rs.rs_sort_profiled(d, ev)[0] == 0
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
+        for ev in steps:
+            st, kinds = rs.rs_sort_profiled(d, ev)
+            assert st == 0
+    kout.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert [rs.KERNEL_KINDS[k] for k in kinds] == ["upsweep", "spine_scan", "downsweep"] * 4
+    for ev in steps:
+        times = [ev[i].elapsed_time(ev[i + 1]) for i in range(len(kinds))]
+        assert all(t > 0 for t in times)
+    assert np.array_equal(kout.cpu().numpy().view(np.uint32), oracle.sort("u32", keys)[0])
+    assert rs.rs_device_status(temp) == 0
+
+
 def test_host_buffer_entry_point():
     n = 200_001
     keys = synth.u64_uniform(n, 60)
