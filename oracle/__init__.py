@@ -7,8 +7,8 @@ single-threaded C, compiled on first use with the host C compiler); this file
 only marshals numpy arrays.
 
 Functions:
-  sort(key_type, keys, values=None, begin_bit=0, end_bit=None, radix_bits=8)
-      LSD radix sort by counting-sort passes ("Radix sort を実装 & 測定してみた",
+  sort(key_type, keys, values=None, begin_bit=0, end_bit=None, radix_bits=8, descending=False)
+      LSD radix sort by counting-sort passes (key types u32 i32 f32 u64 u16 i16 f16) ("Radix sort を実装 & 測定してみた",
       section アルゴリズムの詳細; "Radix sort paralelo sobre el scan", section
       Las tres fases de una pasada).
   one_bit_split_sort(...)
@@ -41,9 +41,10 @@ _LIB = os.path.join(_LIBDIR, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-KEY_TYPES = {"u32": 0, "i32": 1, "f32": 2, "u64": 3}
-KEY_DTYPE = {"u32": np.uint32, "i32": np.uint32, "f32": np.uint32, "u64": np.uint64}
-KEY_BITS = {"u32": 32, "i32": 32, "f32": 32, "u64": 64}
+KEY_TYPES = {"u32": 0, "i32": 1, "f32": 2, "u64": 3, "u16": 4, "i16": 5, "f16": 6}
+KEY_DTYPE = {"u32": np.uint32, "i32": np.uint32, "f32": np.uint32, "u64": np.uint64,
+             "u16": np.uint16, "i16": np.uint16, "f16": np.uint16}
+KEY_BITS = {"u32": 32, "i32": 32, "f32": 32, "u64": 64, "u16": 16, "i16": 16, "f16": 16}
 
 
 def build(force: bool = False) -> str:
@@ -61,6 +62,8 @@ def _bind(lib):
     vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
     lib.oracle_lsd_sort.argtypes = [i32, vp, vp, vp, vp, sz, i32, i32, i32]
     lib.oracle_lsd_sort.restype = i32
+    lib.oracle_lsd_sort_dir.argtypes = [i32, vp, vp, vp, vp, sz, i32, i32, i32, i32]
+    lib.oracle_lsd_sort_dir.restype = i32
     lib.oracle_one_bit_split_sort.argtypes = [i32, vp, vp, vp, vp, sz, i32, i32]
     lib.oracle_one_bit_split_sort.restype = i32
     lib.oracle_decimal_lsd_trace.argtypes = [vp, sz, i32, vp]
@@ -93,8 +96,9 @@ def _vp(a):
 
 
 def sort(key_type: str, keys, values=None, begin_bit: int = 0, end_bit: int | None = None,
-         radix_bits: int = 8, lib=None):
-    """Stable LSD radix sort; returns (keys_out, values_out or None) as new arrays."""
+         radix_bits: int = 8, lib=None, descending: bool = False):
+    """Stable LSD radix sort, ascending or descending (ties in input order);
+    returns (keys_out, values_out or None) as new arrays."""
     k = _as_keys(key_type, keys)
     end_bit = KEY_BITS[key_type] if end_bit is None else end_bit
     n = k.size
@@ -103,8 +107,8 @@ def sort(key_type: str, keys, values=None, begin_bit: int = 0, end_bit: int | No
     vo = None if vi is None else np.empty_like(vi)
     if vi is not None and vi.size != n:
         raise ValueError("values must match keys in length")
-    rc = (lib or _load()).oracle_lsd_sort(KEY_TYPES[key_type], _vp(k), _vp(ko), _vp(vi), _vp(vo), n,
-                                 begin_bit, end_bit, radix_bits)
+    rc = (lib or _load()).oracle_lsd_sort_dir(KEY_TYPES[key_type], _vp(k), _vp(ko), _vp(vi), _vp(vo), n,
+                                              begin_bit, end_bit, radix_bits, int(bool(descending)))
     if rc != 0:
         raise ValueError(f"oracle_lsd_sort failed with code {rc}")
     return ko, vo

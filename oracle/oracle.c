@@ -13,8 +13,8 @@
  *
  * What it computes: for key type t and bit range [begin, end) the unique
  * stable permutation that orders D(i) = bits [begin, end) of the ordered key
- * T_t(key_i) ascending, ties kept in input order.  Output keys are the
- * original bit patterns; output values follow their keys.
+ * T_t(key_i) ascending (or descending), ties kept in input order.  Output keys
+ * are the original bit patterns; output values follow their keys.
  *
  * Readings of the pages taken here (each pinned by the tests):
  *  - int32: the order-preserving map is the sign-bit flip of [P2] "Claves con
@@ -25,13 +25,22 @@
  *    infinities map to 0xFFFFFFFF (all tie, sort last, stable); otherwise a
  *    set sign bit flips every bit and a clear one sets the MSB.
  *  - A digit that would run past end_bit is cut to the remaining bits.
+ *  - 16-bit keys (uint16, int16, IEEE binary16) follow "by the same
+ *    procedure" ([P1] "符号付型、浮動小数点型に対する radix sort" says 16- and
+ *    64-bit keys sort the same way): the int16 map flips the sign bit, the
+ *    binary16 map is [P1]'s float rule at 16 bits (exponent field all ones
+ *    -> 0xFFFF; negative -> all bits flipped; positive -> MSB set).
+ *  - Descending order is the ascending order of the complemented ordered key
+ *    restricted to [begin, end): each pass's counting sort takes its buckets
+ *    in reverse (digit ^ mask), still walking the input in order, so ties
+ *    keep their input order.  (The pages sort ascending only.)
  */
 #include <stddef.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 
-enum { OR_U32 = 0, OR_I32 = 1, OR_F32 = 2, OR_U64 = 3 };
+enum { OR_U32 = 0, OR_I32 = 1, OR_F32 = 2, OR_U64 = 3, OR_U16 = 4, OR_I16 = 5, OR_F16 = 6 };
 
 enum { OR_OK = 0, OR_BAD_ARG = 1, OR_NO_MEMORY = 2 };
 
@@ -54,29 +63,62 @@ uint32_t oracle_ordered_f32(uint32_t bits)
     return bits ^ 0x80000000u;
 }
 
+/* The int16 map: the sign-bit flip of [P2] at 16 bits. */
+uint32_t oracle_ordered_i16(uint32_t bits)
+{
+    return (bits ^ 0x8000u) & 0xFFFFu;
+}
+
+/* The binary16 map: [P1]'s FloatToOrderedUint rule at 16 bits (5-bit
+ * exponent field in bits 10..14). */
+uint32_t oracle_ordered_f16(uint32_t bits)
+{
+    bits &= 0xFFFFu;
+    if ((bits & 0x7C00u) == 0x7C00u)
+        return 0xFFFFu;
+    if (bits & 0x8000u)
+        return ~bits & 0xFFFFu;
+    return bits ^ 0x8000u;
+}
+
 uint64_t oracle_ordered_key(int key_type, uint64_t raw)
 {
     switch (key_type) {
     case OR_U32: return raw & 0xFFFFFFFFull;
     case OR_I32: return oracle_ordered_i32((uint32_t)raw);
     case OR_F32: return oracle_ordered_f32((uint32_t)raw);
+    case OR_U16: return raw & 0xFFFFull;
+    case OR_I16: return oracle_ordered_i16((uint32_t)raw);
+    case OR_F16: return oracle_ordered_f16((uint32_t)raw);
     default:     return raw;
     }
 }
 
-static int key_bits(int key_type) { return key_type == OR_U64 ? 64 : 32; }
-static size_t key_size(int key_type) { return key_type == OR_U64 ? 8 : 4; }
+static int valid_key_type(int key_type) { return key_type >= OR_U32 && key_type <= OR_F16; }
+
+static int key_bits(int key_type)
+{
+    return key_type == OR_U64 ? 64 : key_type >= OR_U16 ? 16 : 32;
+}
+
+static size_t key_size(int key_type) { return (size_t)key_bits(key_type) / 8; }
 
 static uint64_t load_raw(int key_type, const void* keys, size_t i)
 {
-    if (key_type == OR_U64) return ((const uint64_t*)keys)[i];
-    return ((const uint32_t*)keys)[i];
+    switch (key_size(key_type)) {
+    case 8: return ((const uint64_t*)keys)[i];
+    case 2: return ((const uint16_t*)keys)[i];
+    default: return ((const uint32_t*)keys)[i];
+    }
 }
 
 static void store_raw(int key_type, void* keys, size_t i, uint64_t v)
 {
-    if (key_type == OR_U64) ((uint64_t*)keys)[i] = v;
-    else ((uint32_t*)keys)[i] = (uint32_t)v;
+    switch (key_size(key_type)) {
+    case 8: ((uint64_t*)keys)[i] = v; break;
+    case 2: ((uint16_t*)keys)[i] = (uint16_t)v; break;
+    default: ((uint32_t*)keys)[i] = (uint32_t)v; break;
+    }
 }
 
 /* [P5] "CPU上的扫描", written in its exclusive form: out[i] = sum of in[0..i). */
@@ -118,14 +160,15 @@ static void counting_pass(const uint64_t* src_keys, const uint32_t* src_vals,
  * first ([P1] "アルゴリズムの詳細"; [P2] "Las tres fases de una pasada"; [P3]
  * 13.2).  Pass p sorts by bits [begin + p*r, min(begin + (p+1)*r, end)) of the
  * ordered key, recomputed from the original bits in every pass as [P1]'s CPU
- * code does, so the output keeps the original bit patterns.
+ * code does, so the output keeps the original bit patterns.  With descending
+ * set, each pass takes its buckets in reverse order (digit ^ mask).
  * vals_in / vals_out may both be NULL (keys only).
  */
-int oracle_lsd_sort(int key_type, const void* keys_in, void* keys_out,
-                    const uint32_t* vals_in, uint32_t* vals_out, size_t n,
-                    int begin_bit, int end_bit, int radix_bits)
+int oracle_lsd_sort_dir(int key_type, const void* keys_in, void* keys_out,
+                        const uint32_t* vals_in, uint32_t* vals_out, size_t n,
+                        int begin_bit, int end_bit, int radix_bits, int descending)
 {
-    if (key_type < OR_U32 || key_type > OR_U64) return OR_BAD_ARG;
+    if (!valid_key_type(key_type)) return OR_BAD_ARG;
     if (begin_bit < 0 || end_bit < begin_bit || end_bit > key_bits(key_type)) return OR_BAD_ARG;
     if (radix_bits < 1 || radix_bits > 16) return OR_BAD_ARG;
     if ((vals_in == NULL) != (vals_out == NULL)) return OR_BAD_ARG;
@@ -150,8 +193,9 @@ int oracle_lsd_sort(int key_type, const void* keys_in, void* keys_out,
     for (int lo = begin_bit; lo < end_bit; lo += radix_bits) {
         int width = end_bit - lo < radix_bits ? end_bit - lo : radix_bits;
         uint64_t mask = (width == 64) ? ~0ull : ((1ull << width) - 1);
+        const uint64_t flip = descending ? mask : 0;
         for (size_t i = 0; i < n; ++i)
-            digit[i] = (uint32_t)((oracle_ordered_key(key_type, a[i]) >> lo) & mask);
+            digit[i] = (uint32_t)(((oracle_ordered_key(key_type, a[i]) >> lo) & mask) ^ flip);
         counting_pass(a, va, digit, n, nbins, b, vb, count, start);
         uint64_t* t = a; a = b; b = t;
         uint32_t* tv = va; va = vb; vb = tv;
@@ -161,6 +205,14 @@ int oracle_lsd_sort(int key_type, const void* keys_in, void* keys_out,
 done:
     free(a); free(b); free(va); free(vb); free(digit); free(count); free(start);
     return rc;
+}
+
+int oracle_lsd_sort(int key_type, const void* keys_in, void* keys_out,
+                    const uint32_t* vals_in, uint32_t* vals_out, size_t n,
+                    int begin_bit, int end_bit, int radix_bits)
+{
+    return oracle_lsd_sort_dir(key_type, keys_in, keys_out, vals_in, vals_out, n, begin_bit, end_bit,
+                               radix_bits, 0);
 }
 
 /*
@@ -202,7 +254,7 @@ int oracle_one_bit_split_sort(int key_type, const void* keys_in, void* keys_out,
                               const uint32_t* vals_in, uint32_t* vals_out, size_t n,
                               int begin_bit, int end_bit)
 {
-    if (key_type < OR_U32 || key_type > OR_U64) return OR_BAD_ARG;
+    if (!valid_key_type(key_type)) return OR_BAD_ARG;
     if (begin_bit < 0 || end_bit < begin_bit || end_bit > key_bits(key_type)) return OR_BAD_ARG;
     if ((vals_in == NULL) != (vals_out == NULL)) return OR_BAD_ARG;
     if (n == 0) return OR_OK;

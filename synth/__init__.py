@@ -138,6 +138,39 @@ def f32_edge(n: int, seed: int, out=None):
     return out
 
 
+def u16_uniform(n: int, seed: int, out=None):
+    """16-bit keys: the low halves of the uint32 stream of the same seed."""
+    out = _out(out, n, np.uint16)
+    out[:n] = (u32_uniform(n, seed) & np.uint32(0xFFFF)).astype(np.uint16)
+    return out
+
+
+# binary16 boundary patterns: zeros, subnormals, the smallest normal, +-1,
+# the largest finite, infinities and NaN payloads of both signs.
+F16_BOUNDARY = np.array([0x0000, 0x8000, 0x0001, 0x8001, 0x03FF, 0x83FF, 0x0400, 0x8400, 0x3C00,
+                         0xBC00, 0x3C01, 0xBC01, 0x7BFF, 0xFBFF, 0x7C00, 0xFC00, 0x7E00, 0xFE00,
+                         0x7C01, 0xFC01, 0x7FFF, 0xFFFF, 0x4248, 0xC248], dtype=np.uint16)
+
+
+def f16_edge(n: int, seed: int, out=None):
+    """binary16 bit patterns: every third key a boundary pattern, the rest
+    random bits (any class: normal, subnormal, zero, Inf, NaN)."""
+    out = _out(out, n, np.uint16)
+    rnd = (u32_uniform(n, seed) & np.uint32(0xFFFF)).astype(np.uint16)
+    pick = u32_uniform(n, seed ^ 0x16) % np.uint32(3 * len(F16_BOUNDARY))
+    out[:n] = np.where(pick < len(F16_BOUNDARY), F16_BOUNDARY[np.minimum(pick, len(F16_BOUNDARY) - 1)], rnd)
+    return out
+
+
+def f16_normal_specials(n: int, seed: int, out=None):
+    """binary16 bit patterns of N(0,1) values (the float32 generator's values
+    rounded to half precision, its injected -0.0, +0.0, +-Inf and NaN kept)."""
+    out = _out(out, n, np.uint16)
+    f = f32_normal_specials(n, seed).view(np.float32)
+    out[:n] = f.astype(np.float16).view(np.uint16)
+    return out
+
+
 # ---------------------------------------------------------------- workloads
 
 @dataclass(frozen=True)

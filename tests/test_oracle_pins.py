@@ -19,7 +19,13 @@ passed as ``lib``) against something other than itself:
   scan", section "Claves con signo y en coma flotante"), checked against IEEE
   and two's-complement order with Python's own comparisons;
 * brute force: Python's stable ``sorted`` on tiny and small inputs, exhaustive
-  over 3-value alphabets.
+  over 3-value alphabets;
+* 16-bit keys (uint16, int16 and IEEE binary16, sorted "by the same
+  procedure" as "Radix sort を実装 & 測定してみた" says of other widths): the
+  maps' ordering invariants against Python's half-precision unpacking and
+  two's-complement values, and brute force;
+* descending order against Python's stable ``sorted(..., reverse=True)``,
+  which keeps ties in input order.
 
 ``test_planted_mistakes_are_caught`` compiles copies of oracle.c with one
 plausible mistake each and checks that some pin fails for every copy.
@@ -53,21 +59,36 @@ def f32_order_key(bits: int):
     return (1, v, 0)
 
 
+def f16_order_key(bits: int):
+    """The same total order for IEEE binary16 (Python unpacks half precision)."""
+    if (bits >> 10) & 0x1F == 0x1F:
+        return (2, 0.0, 0)
+    v = struct.unpack("<e", struct.pack("<H", bits))[0]
+    if v == 0.0:
+        return (1, 0.0, -1 if bits & 0x8000 else 0)
+    return (1, v, 0)
+
+
 def i32_value(bits: int) -> int:
     return bits - (1 << 32) if bits & 0x80000000 else bits
 
 
-def brute_force_perm(key_type, keys, begin_bit, end_bit):
-    """Stable order of indices by the definition of the sort (Python's sort is stable)."""
+def i16_value(bits: int) -> int:
+    return bits - (1 << 16) if bits & 0x8000 else bits
+
+
+def brute_force_perm(key_type, keys, begin_bit, end_bit, descending=False):
+    """Stable order of indices by the definition of the sort (Python's sort is
+    stable, also with reverse=True)."""
     n = len(keys)
     full = begin_bit == 0 and end_bit == oracle.KEY_BITS[key_type]
-    if key_type == "f32" and full:
-        return sorted(range(n), key=lambda i: f32_order_key(int(keys[i])))
-    if key_type == "i32" and full:
-        return sorted(range(n), key=lambda i: i32_value(int(keys[i])))
-    if key_type in ("u32", "u64"):
+    by = {"f32": f32_order_key, "f16": f16_order_key, "i32": i32_value, "i16": i16_value}
+    if key_type in by and full:
+        f = by[key_type]
+        return sorted(range(n), key=lambda i: f(int(keys[i])), reverse=descending)
+    if key_type in ("u32", "u64", "u16"):
         mask = (1 << (end_bit - begin_bit)) - 1
-        return sorted(range(n), key=lambda i: (int(keys[i]) >> begin_bit) & mask)
+        return sorted(range(n), key=lambda i: (int(keys[i]) >> begin_bit) & mask, reverse=descending)
     raise ValueError("no independent order for a partial bit range of a signed/float key")
 
 
@@ -211,14 +232,16 @@ def pin_i32_invariants(lib=None):
             assert (ordk[i] < ordk[j]) == (vals[i] < vals[j]), (hex(table[i]), hex(table[j]))
 
 
-def _check_against_brute(key_type, keys, begin_bit, end_bit, lib=None, radix_bits=8):
+def _check_against_brute(key_type, keys, begin_bit, end_bit, lib=None, radix_bits=8, descending=False):
     n = len(keys)
     vals = np.arange(n, dtype=np.uint32)
-    want = brute_force_perm(key_type, keys, begin_bit, end_bit)
-    ko, vo = oracle.sort(key_type, keys, vals, begin_bit, end_bit, radix_bits=radix_bits, lib=lib)
+    want = brute_force_perm(key_type, keys, begin_bit, end_bit, descending)
+    ko, vo = oracle.sort(key_type, keys, vals, begin_bit, end_bit, radix_bits=radix_bits, lib=lib,
+                         descending=descending)
     assert vo.tolist() == want
     assert ko.tolist() == [int(keys[i]) for i in want]
-    ko2, _ = oracle.sort(key_type, keys, None, begin_bit, end_bit, radix_bits=radix_bits, lib=lib)
+    ko2, _ = oracle.sort(key_type, keys, None, begin_bit, end_bit, radix_bits=radix_bits, lib=lib,
+                         descending=descending)
     assert np.array_equal(ko, ko2)
 
 
@@ -257,6 +280,69 @@ def pin_exhaustive_tiny(lib=None):
                 _check_against_brute(kt, np.array(combo, dtype=dt), 0, oracle.KEY_BITS[kt], lib)
 
 
+BOUNDARY_I16 = [0x8000, 0x8001, 0xFFFE, 0xFFFF, 0, 1, 2, 0x7FFE, 0x7FFF, 0x0100, 0xFF00, 0x4000, 0xC000]
+
+
+def pin_f16_invariants(lib=None):
+    table = [int(v) for v in synth.F16_BOUNDARY] + [int(v) for v in synth.f16_edge(150, 78)]
+    keys = np.array(table, dtype=np.uint16)
+    ordk = oracle.ordered_keys("f16", keys, lib=lib).tolist()
+    ref = [f16_order_key(b) for b in table]
+    for i in range(len(table)):
+        for j in range(len(table)):
+            assert (ordk[i] < ordk[j]) == (ref[i] < ref[j]), (hex(table[i]), hex(table[j]))
+            assert (ordk[i] == ordk[j]) == (ref[i] == ref[j]), (hex(table[i]), hex(table[j]))
+    for b in table:
+        special = ((b >> 10) & 0x1F) == 0x1F
+        assert (int(oracle.ordered_keys("f16", np.array([b], np.uint16), lib=lib)[0]) == 0xFFFF) == special
+
+
+def pin_i16_invariants(lib=None):
+    table = BOUNDARY_I16 + [int(v) for v in synth.u16_uniform(100, 22)]
+    ordk = oracle.ordered_keys("i16", np.array(table, dtype=np.uint16), lib=lib).tolist()
+    vals = [i16_value(b) for b in table]
+    for i in range(len(table)):
+        for j in range(len(table)):
+            assert (ordk[i] < ordk[j]) == (vals[i] < vals[j]), (hex(table[i]), hex(table[j]))
+
+
+def pin_brute_force_16bit(lib=None):
+    rng = np.random.default_rng(99)
+    for n in (0, 1, 2, 31, 300, 2000):
+        u16 = synth.u16_uniform(n, 500 + n)
+        _check_against_brute("u16", u16, 0, 16, lib)
+        _check_against_brute("u16", u16 & np.uint16(0x0F0F), 0, 16, lib)     # many ties
+        b = int(rng.integers(0, 16))
+        e = int(rng.integers(b, 17))
+        _check_against_brute("u16", u16, b, e, lib)
+        _check_against_brute("i16", u16, 0, 16, lib)
+        _check_against_brute("f16", synth.f16_edge(n, 600 + n), 0, 16, lib)
+        _check_against_brute("f16", synth.f16_normal_specials(n, 700 + n), 0, 16, lib, radix_bits=4)
+
+
+def pin_descending(lib=None):
+    rng = np.random.default_rng(7)
+    for n in (0, 1, 2, 3, 64, 777):
+        u32 = synth.u32_uniform(n, 800 + n)
+        _check_against_brute("u32", u32, 0, 32, lib, descending=True)
+        _check_against_brute("u32", synth.u32_bits(n, 801 + n, 4), 0, 32, lib, descending=True)  # ties
+        b = int(rng.integers(0, 32))
+        e = int(rng.integers(b, 33))
+        _check_against_brute("u32", u32, b, e, lib, descending=True, radix_bits=5)
+        _check_against_brute("i32", u32, 0, 32, lib, descending=True)
+        _check_against_brute("f32", synth.f32_edge(n, 802 + n), 0, 32, lib, descending=True)
+        _check_against_brute("u64", synth.u64_uniform(n, 803 + n), 0, 64, lib, descending=True)
+        _check_against_brute("u16", synth.u16_uniform(n, 804 + n), 3, 13, lib, descending=True)
+        _check_against_brute("i16", synth.u16_uniform(n, 805 + n), 0, 16, lib, descending=True)
+        _check_against_brute("f16", synth.f16_edge(n, 806 + n), 0, 16, lib, descending=True)
+    for kt, letters in {"u32": [0, 7, 0xFFFFFFFF], "f16": [0x8000, 0x0000, 0x7E00]}.items():
+        dt = oracle.KEY_DTYPE[kt]
+        for n in range(0, 6):
+            for combo in itertools.product(letters, repeat=n):
+                _check_against_brute(kt, np.array(combo, dtype=dt), 0, oracle.KEY_BITS[kt], lib,
+                                     descending=True)
+
+
 def pin_f32_specials_keep_order(lib=None):
     # -Inf, +Inf and NaNs of any payload all tie at the top and keep input order
     keys = np.array([0x7FC00000, 0x3F800000, 0xFF800000, 0x7F800000, 0xBF800000, 0xFFC00001,
@@ -267,7 +353,8 @@ def pin_f32_specials_keep_order(lib=None):
 
 ALL_PINS = [pin_decimal_example, pin_one_bit_split, pin_global_position, pin_digit_major_scan,
             pin_blelloch_scan, pin_f32_invariants, pin_i32_invariants, pin_brute_force,
-            pin_exhaustive_tiny, pin_f32_specials_keep_order]
+            pin_exhaustive_tiny, pin_f32_specials_keep_order, pin_f16_invariants,
+            pin_i16_invariants, pin_brute_force_16bit, pin_descending]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda p: p.__name__)
@@ -319,6 +406,16 @@ MUTANTS = {
     # does not cut the last digit at end_bit
     "last_digit_uncut": ("int width = end_bit - lo < radix_bits ? end_bit - lo : radix_bits;",
                          "int width = radix_bits;"),
+    # drops the NaN/Inf rule of the binary16 map
+    "no_special_values_f16": ("    if ((bits & 0x7C00u) == 0x7C00u)\n        return 0xFFFFu;\n", ""),
+    # flips all bits of negative int16 keys
+    "int16_flip_all": ("    return (bits ^ 0x8000u) & 0xFFFFu;",
+                       "    return (bits & 0x8000u) ? (~bits & 0xFFFFu) : (bits ^ 0x8000u);"),
+    # sorts ascending whatever was asked
+    "descending_ignored": ("const uint64_t flip = descending ? mask : 0;", "const uint64_t flip = 0;"),
+    # reverses only the lowest digit (a per-pass mistake the full-key checks see)
+    "descending_first_pass_only": ("const uint64_t flip = descending ? mask : 0;",
+                                   "const uint64_t flip = (descending && lo == begin_bit) ? mask : 0;"),
     # one-bit split fills the ones from the back (a permutation, but not stable)
     "one_bit_ones_reversed": ("uint64_t dst = one ? F + (uint64_t)i - s[i] : s[i];",
                               "uint64_t dst = one ? (uint64_t)n - 1 - ((uint64_t)i - s[i]) : s[i];"),

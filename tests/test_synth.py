@@ -71,3 +71,16 @@ def test_workload_table():
     small = w["c3_i32_2p26"].keys(n=1000)
     assert small.dtype == np.uint32 and small.size == 1000
     assert synth.sweep_workload(20).n == 1 << 20
+
+
+def test_16bit_generators_are_seeded_and_prefix_stable():
+    for gen in (synth.u16_uniform, synth.f16_edge, synth.f16_normal_specials):
+        a = gen(1000, 5)
+        assert a.dtype == np.uint16 and a.size == 1000
+        assert np.array_equal(a, gen(1000, 5))
+        assert not np.array_equal(a, gen(1000, 6))
+    # the half-precision normals keep the float32 generator's injected specials
+    f = synth.f16_normal_specials(100_000, 9)
+    exp = (f >> 10) & 0x1F
+    assert np.any(f == 0x8000) and np.any(f == 0) and np.any(f == 0x7C00) and np.any(f == 0xFC00)
+    assert np.any((exp == 0x1F) & ((f & 0x3FF) != 0))
