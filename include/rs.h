@@ -2,20 +2,24 @@
  * rs.h -- C ABI of a stable least-significant-digit radix sort for NVIDIA
  * GB300 (sm_103a).
  *
- * What is computed.  For n keys of one type (uint32, int32, float32 or
- * uint64) and a bit range [begin_bit, end_bit), the sort returns the keys,
- * and optionally one uint32 value per key, in the unique STABLE order of
+ * What is computed.  For n keys of one type (uint32, int32, float32, uint64,
+ * uint16, int16 or binary16) and a bit range [begin_bit, end_bit), the sort
+ * returns the keys, and optionally one uint32 value per key, in the unique
+ * STABLE order of
  *     D(i) = bits [begin_bit, end_bit) of T(key_i),
- * ascending, ties kept in input order.  T is the order-preserving map to an
- * unsigned integer:
- *   - uint32, uint64: identity;
- *   - int32: flip the sign bit ("Radix sort paralelo sobre el scan", section
- *     "Claves con signo y en coma flotante");
+ * ascending (descending on request, rs_sort_desc.descending), ties kept in
+ * input order either way.  T is the order-preserving map to an unsigned
+ * integer:
+ *   - uint32, uint64, uint16: identity;
+ *   - int32, int16: flip the sign bit ("Radix sort paralelo sobre el scan",
+ *     section "Claves con signo y en coma flotante");
  *   - float32: NaN (any payload, either sign) and +-Inf map to 0xFFFFFFFF;
  *     otherwise a set sign bit flips every bit and a clear one sets the MSB
  *     ("Radix sort を実装 & 測定してみた", section "符号付型、浮動小数点型に
  *     対する radix sort").  So -Inf, +Inf and all NaNs tie after every finite
- *     value, in input order, and -0.0 sorts just before +0.0.
+ *     value, in input order, and -0.0 sorts just before +0.0;
+ *   - binary16: the same rule at 16 bits (that section says other widths
+ *     sort by the same procedure): exponent field all ones -> 0xFFFF.
  * The output keys are the ORIGINAL bit patterns (nothing is re-encoded).  Bits
  * outside [begin_bit, end_bit) of T(key) do not influence the order.
  *
@@ -84,7 +88,10 @@ typedef enum rs_status {
     RS_ERR_UNSUPPORTED = 7     /* valid request this build does not handle             */
 } rs_status;
 
-typedef enum rs_key_type { RS_U32 = 0, RS_I32 = 1, RS_F32 = 2, RS_U64 = 3 } rs_key_type;
+typedef enum rs_key_type {
+    RS_U32 = 0, RS_I32 = 1, RS_F32 = 2, RS_U64 = 3,
+    RS_U16 = 4, RS_I16 = 5, RS_F16 = 6  /* 16-bit keys; F16 = IEEE binary16 bit patterns */
+} rs_key_type;
 
 typedef enum rs_algo {
     RS_ALGO_AUTO = 0,        /* the cluster sort for n <= rs_cluster_max_n(),
@@ -115,6 +122,13 @@ rs_status rs_sort_keys_f32(const float* keys_in, float* keys_out, size_t n,
                            int begin_bit, int end_bit, void* temp, size_t temp_bytes, void* stream);
 rs_status rs_sort_keys_u64(const uint64_t* keys_in, uint64_t* keys_out, size_t n,
                            int begin_bit, int end_bit, void* temp, size_t temp_bytes, void* stream);
+rs_status rs_sort_keys_u16(const uint16_t* keys_in, uint16_t* keys_out, size_t n,
+                           int begin_bit, int end_bit, void* temp, size_t temp_bytes, void* stream);
+rs_status rs_sort_keys_i16(const int16_t* keys_in, int16_t* keys_out, size_t n,
+                           int begin_bit, int end_bit, void* temp, size_t temp_bytes, void* stream);
+/* binary16 keys as their 16-bit patterns */
+rs_status rs_sort_keys_f16(const uint16_t* keys_in, uint16_t* keys_out, size_t n,
+                           int begin_bit, int end_bit, void* temp, size_t temp_bytes, void* stream);
 
 /* Keys with one uint32 value each ("Radix sort paralelo sobre el scan": the
  * payload travels with its key).  vals_in / vals_out: n values. */
@@ -128,6 +142,15 @@ rs_status rs_sort_pairs_f32(const float* keys_in, float* keys_out, const uint32_
                             uint32_t* vals_out, size_t n, int begin_bit, int end_bit,
                             void* temp, size_t temp_bytes, void* stream);
 rs_status rs_sort_pairs_u64(const uint64_t* keys_in, uint64_t* keys_out, const uint32_t* vals_in,
+                            uint32_t* vals_out, size_t n, int begin_bit, int end_bit,
+                            void* temp, size_t temp_bytes, void* stream);
+rs_status rs_sort_pairs_u16(const uint16_t* keys_in, uint16_t* keys_out, const uint32_t* vals_in,
+                            uint32_t* vals_out, size_t n, int begin_bit, int end_bit,
+                            void* temp, size_t temp_bytes, void* stream);
+rs_status rs_sort_pairs_i16(const int16_t* keys_in, int16_t* keys_out, const uint32_t* vals_in,
+                            uint32_t* vals_out, size_t n, int begin_bit, int end_bit,
+                            void* temp, size_t temp_bytes, void* stream);
+rs_status rs_sort_pairs_f16(const uint16_t* keys_in, uint16_t* keys_out, const uint32_t* vals_in,
                             uint32_t* vals_out, size_t n, int begin_bit, int end_bit,
                             void* temp, size_t temp_bytes, void* stream);
 
@@ -156,6 +179,8 @@ typedef struct rs_sort_desc {
      * waits behind it run out and the sort reports RS_ERR_DEVICE_TIMEOUT. */
     uint32_t spin_limit;
     int32_t stall_tile;
+    /* 1: descending order of D (ties still in input order); 0: ascending. */
+    int descending;
 } rs_sort_desc;
 
 rs_status rs_sort(const rs_sort_desc* desc);

@@ -17,9 +17,9 @@ import os
 
 from . import _build
 
-KEY_TYPES = {"u32": 0, "i32": 1, "f32": 2, "u64": 3}
-KEY_BYTES = {"u32": 4, "i32": 4, "f32": 4, "u64": 8}
-KEY_BITS = {"u32": 32, "i32": 32, "f32": 32, "u64": 64}
+KEY_TYPES = {"u32": 0, "i32": 1, "f32": 2, "u64": 3, "u16": 4, "i16": 5, "f16": 6}
+KEY_BYTES = {"u32": 4, "i32": 4, "f32": 4, "u64": 8, "u16": 2, "i16": 2, "f16": 2}
+KEY_BITS = {k: 8 * b for k, b in KEY_BYTES.items()}
 ALGOS = {"auto": 0, "onesweep": 1, "reduce_scan": 2, "cluster": 3}
 STATUS = {0: "RS_OK", 1: "RS_ERR_INVALID_ARG", 2: "RS_ERR_TEMP_TOO_SMALL", 3: "RS_ERR_ALIAS",
           4: "RS_ERR_CUDA", 5: "RS_ERR_DEVICE_TIMEOUT", 6: "RS_ERR_CHECK_FAILED",
@@ -43,7 +43,8 @@ class SortDesc(ctypes.Structure):
                 ("begin_bit", ctypes.c_int), ("end_bit", ctypes.c_int), ("algo", ctypes.c_int),
                 ("radix_bits", ctypes.c_int), ("temp", ctypes.c_void_p),
                 ("temp_bytes", ctypes.c_size_t), ("stream", ctypes.c_void_p),
-                ("spin_limit", ctypes.c_uint32), ("stall_tile", ctypes.c_int32)]
+                ("spin_limit", ctypes.c_uint32), ("stall_tile", ctypes.c_int32),
+                ("descending", ctypes.c_int)]
 
 
 _lib = None
@@ -70,7 +71,7 @@ SIGNATURES = {
 }
 SIGNATURES["rs_sort_keys_u32_noalloc"] = (_i, [_vp, _vp, _sz, _i, _i, _vp])
 NOALLOC_MAX_N = 1 << 22
-for _t in ("u32", "i32", "f32", "u64"):
+for _t in ("u32", "i32", "f32", "u64", "u16", "i16", "f16"):
     SIGNATURES[f"rs_sort_keys_{_t}"] = _KEYS_SIG
     SIGNATURES[f"rs_sort_pairs_{_t}"] = _PAIRS_SIG
 
@@ -152,6 +153,9 @@ rs_sort_keys_u32, rs_sort_pairs_u32 = _typed("u32")
 rs_sort_keys_i32, rs_sort_pairs_i32 = _typed("i32")
 rs_sort_keys_f32, rs_sort_pairs_f32 = _typed("f32")
 rs_sort_keys_u64, rs_sort_pairs_u64 = _typed("u64")
+rs_sort_keys_u16, rs_sort_pairs_u16 = _typed("u16")
+rs_sort_keys_i16, rs_sort_pairs_i16 = _typed("i16")
+rs_sort_keys_f16, rs_sort_pairs_f16 = _typed("f16")
 
 
 def rs_sort_keys_u32_noalloc(keys_in, keys_out, n, begin_bit, end_bit, stream=None):
@@ -162,10 +166,11 @@ def rs_sort_keys_u32_noalloc(keys_in, keys_out, n, begin_bit, end_bit, stream=No
 
 
 def make_desc(key_type, keys_in, keys_out, vals_in, vals_out, n, begin_bit, end_bit, temp,
-              temp_bytes, stream=None, algo="auto", radix_bits=0, spin_limit=0, stall_tile=0):
+              temp_bytes, stream=None, algo="auto", radix_bits=0, spin_limit=0, stall_tile=0,
+              descending=False):
     return SortDesc(KEY_TYPES[key_type], _addr(keys_in), _addr(keys_out), _addr(vals_in),
                     _addr(vals_out), n, begin_bit, end_bit, ALGOS[algo], radix_bits, _addr(temp),
-                    temp_bytes, _stream(stream), spin_limit, stall_tile)
+                    temp_bytes, _stream(stream), spin_limit, stall_tile, int(bool(descending)))
 
 
 def rs_sort(desc: SortDesc) -> int:
@@ -239,8 +244,8 @@ class Graph:
 
 def key_type_of(t) -> str:
     import torch
-    m = {torch.int32: "i32", torch.float32: "f32"}
-    for name in ("uint32", "uint64"):
+    m = {torch.int32: "i32", torch.float32: "f32", torch.int16: "i16", torch.float16: "f16"}
+    for name in ("uint32", "uint64", "uint16"):
         dt = getattr(torch, name, None)
         if dt is not None:
             m[dt] = "u" + name[4:]
@@ -250,8 +255,9 @@ def key_type_of(t) -> str:
 
 
 def sort(keys, values=None, *, key_type=None, begin_bit=0, end_bit=None, algo="auto",
-         radix_bits=0, keys_out=None, values_out=None, temp=None, stream=None):
-    """Stable radix sort of a CUDA tensor of keys (and uint32 values).
+         radix_bits=0, keys_out=None, values_out=None, temp=None, stream=None, descending=False):
+    """Stable radix sort of a CUDA tensor of keys (and uint32 values),
+    ascending or descending (ties keep their input order either way).
 
     Returns (keys_out, values_out or None).  Allocates the outputs and temp
     with torch when they are not given; enqueues on `stream` (default: the
@@ -273,6 +279,6 @@ def sort(keys, values=None, *, key_type=None, begin_bit=0, end_bit=None, algo="a
     if temp is None:
         temp = torch.empty(max(tb, 1), dtype=torch.uint8, device=keys.device)
     desc = make_desc(kt, keys, keys_out, values, values_out, n, begin_bit, end_bit, temp,
-                     temp.numel(), stream, algo, radix_bits)
+                     temp.numel(), stream, algo, radix_bits, descending=descending)
     _check(rs_sort(desc), "rs_sort")
     return keys_out, values_out

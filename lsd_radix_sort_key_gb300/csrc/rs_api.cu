@@ -17,6 +17,9 @@ extern template rs_status run_sort<KU32>(Plan& pl);
 extern template rs_status run_sort<KI32>(Plan& pl);
 extern template rs_status run_sort<KF32>(Plan& pl);
 extern template rs_status run_sort<KU64>(Plan& pl);
+extern template rs_status run_sort<KU16>(Plan& pl);
+extern template rs_status run_sort<KI16>(Plan& pl);
+extern template rs_status run_sort<KF16>(Plan& pl);
 }  // namespace rs
 
 namespace {
@@ -26,9 +29,9 @@ constexpr size_t kOnesweepMaxN = ((size_t)1 << 30) - 1;
 constexpr size_t kAutoReduceScanMinN = (size_t)1 << 25;
 constexpr uint32_t kDefaultSpinLimit = 1u << 20;      // each spin is one L2 round trip (~1 s in all)
 
-int key_bytes(rs_key_type kt) { return kt == RS_U64 ? 8 : 4; }
-int key_bits(rs_key_type kt) { return kt == RS_U64 ? 64 : 32; }
-bool valid_kt(int kt) { return kt >= RS_U32 && kt <= RS_U64; }
+int key_bytes(rs_key_type kt) { return kt == RS_U64 ? 8 : kt >= RS_U16 ? 2 : 4; }
+int key_bits(rs_key_type kt) { return 8 * key_bytes(kt); }
+bool valid_kt(int kt) { return kt >= RS_U32 && kt <= RS_F16; }
 
 bool ranges_overlap(const void* a, size_t abytes, const void* b, size_t bbytes)
 {
@@ -58,6 +61,7 @@ rs_status make_plan(const rs_sort_desc* d, rs::Plan* pl)
         d->algo != RS_ALGO_CLUSTER)
         return RS_ERR_INVALID_ARG;
     if (d->stall_tile < 0) return RS_ERR_INVALID_ARG;
+    if (d->descending != 0 && d->descending != 1) return RS_ERR_INVALID_ARG;
     const size_t n = d->n;
     const int kb = key_bytes(d->key_type);
     *pl = rs::Plan{};
@@ -67,6 +71,7 @@ rs_status make_plan(const rs_sort_desc* d, rs::Plan* pl)
     pl->begin_bit = d->begin_bit;
     pl->end_bit = d->end_bit;
     pl->radix_bits = d->radix_bits == 0 ? 8 : d->radix_bits;
+    pl->descending = d->descending != 0;
     pl->passes = rs::passes_for(d->begin_bit, d->end_bit, pl->radix_bits);
     pl->algo = d->algo;
     const size_t cluster_max = rs::cluster_max_n(kb, vals);
@@ -118,6 +123,9 @@ rs_status dispatch(rs::Plan& pl)
     case RS_U32: return rs::run_sort<rs::KU32>(pl);
     case RS_I32: return rs::run_sort<rs::KI32>(pl);
     case RS_F32: return rs::run_sort<rs::KF32>(pl);
+    case RS_U16: return rs::run_sort<rs::KU16>(pl);
+    case RS_I16: return rs::run_sort<rs::KI16>(pl);
+    case RS_F16: return rs::run_sort<rs::KF16>(pl);
     default:     return rs::run_sort<rs::KU64>(pl);
     }
 }
@@ -252,6 +260,9 @@ RS_TYPED(u32, RS_U32, uint32_t)
 RS_TYPED(i32, RS_I32, int32_t)
 RS_TYPED(f32, RS_F32, float)
 RS_TYPED(u64, RS_U64, uint64_t)
+RS_TYPED(u16, RS_U16, uint16_t)
+RS_TYPED(i16, RS_I16, int16_t)
+RS_TYPED(f16, RS_F16, uint16_t)
 #undef RS_TYPED
 
 rs_status rs_device_status(const void* temp, void* stream)

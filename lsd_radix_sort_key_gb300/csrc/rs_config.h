@@ -66,7 +66,8 @@ constexpr int tile_threads(int algo, int key_bytes, bool vals)
 #endif
 constexpr int tile_items(int key_bytes, bool vals)
 {
-    return key_bytes == 4 ? (vals ? RS_ITEMS_U32_PAIRS : RS_ITEMS_U32_KEYS) : (vals ? 9 : 12);
+    // 16-bit keys live in 32-bit registers: the 32-bit shapes
+    return key_bytes <= 4 ? (vals ? RS_ITEMS_U32_PAIRS : RS_ITEMS_U32_KEYS) : (vals ? 9 : 12);
 }
 constexpr int tile_keys(int algo, int key_bytes, bool vals)
 {
@@ -95,7 +96,7 @@ constexpr int cluster_items(int key_bytes, bool vals)
     // uint32 keys RS_CL_ITEMS per thread; 3/4 of that with values or for
     // uint64 keys, 9/16 for uint64 keys with values (registers and shared
     // memory scale with the bytes per key)
-    return key_bytes == 4 ? (vals ? RS_CL_ITEMS * 3 / 4 : RS_CL_ITEMS)
+    return key_bytes <= 4 ? (vals ? RS_CL_ITEMS * 3 / 4 : RS_CL_ITEMS)
                           : (vals ? RS_CL_ITEMS * 9 / 16 : RS_CL_ITEMS * 3 / 4);
 }
 constexpr size_t cluster_tile_keys(int key_bytes, bool vals)

@@ -101,10 +101,11 @@
 
 namespace rs {
 
-enum : int { KU32 = 0, KI32 = 1, KF32 = 2, KU64 = 3 };
-// The same 32-bit key types, for passes whose digit is one whole byte of the
-// ordered key: the digit is then one byte permute instead of a shift and a mask.
-enum : int { KU32B = 4, KI32B = 5, KF32B = 6 };
+enum : int { KU32 = 0, KI32 = 1, KF32 = 2, KU64 = 3, KU16 = 4, KI16 = 5, KF16 = 6 };
+// The same 32- and 16-bit key types, for passes whose digit is one whole byte
+// of the ordered key: the digit is then one byte permute instead of a shift
+// and a mask.
+enum : int { KU32B = 7, KI32B = 8, KF32B = 9, KU16B = 10, KI16B = 11, KF16B = 12 };
 
 // ------------------------------------------------------------------ key maps
 
@@ -141,20 +142,49 @@ template <> struct KeyOps<KU64> {
     static __device__ __forceinline__ uint64_t ordered(uint64_t u) { return u; }
 };
 
+// 16-bit keys sort "by the same procedure" ("Radix sort を実装 & 測定してみた",
+// section 符号付型、浮動小数点型に対する radix sort): int16 flips its sign bit,
+// binary16 takes the float rule at 16 bits (exponent field all ones -> the
+// maximum; negative -> all bits flipped; positive -> MSB set).
+template <> struct KeyOps<KU16> {
+    using T = uint16_t;
+    static __device__ __forceinline__ uint32_t ordered(uint16_t u) { return u; }
+};
+template <> struct KeyOps<KI16> {
+    using T = uint16_t;
+    static __device__ __forceinline__ uint32_t ordered(uint16_t u) { return (uint32_t)u ^ 0x8000u; }
+};
+template <> struct KeyOps<KF16> {
+    using T = uint16_t;
+    static __device__ __forceinline__ uint32_t ordered(uint16_t h)
+    {
+        const uint32_t u = h;
+        const uint32_t flip = ((u & 0x8000u) ? 0xFFFFu : 0x8000u);
+        return ((u & 0x7C00u) == 0x7C00u) ? 0xFFFFu : (u ^ flip);
+    }
+};
+
 template <> struct KeyOps<KU32B> : KeyOps<KU32> { static constexpr bool kByte = true; };
 template <> struct KeyOps<KI32B> : KeyOps<KI32> { static constexpr bool kByte = true; };
 template <> struct KeyOps<KF32B> : KeyOps<KF32> { static constexpr bool kByte = true; };
+template <> struct KeyOps<KU16B> : KeyOps<KU16> { static constexpr bool kByte = true; };
+template <> struct KeyOps<KI16B> : KeyOps<KI16> { static constexpr bool kByte = true; };
+template <> struct KeyOps<KF16B> : KeyOps<KF16> { static constexpr bool kByte = true; };
 
 template <int KT, typename = void> struct IsByte { static constexpr bool value = false; };
 template <int KT> struct IsByte<KT, decltype((void)KeyOps<KT>::kByte)> { static constexpr bool value = true; };
 
+// The digit of key u for a pass at `shift` of width mask; `flip` (mask for a
+// descending sort, else 0) reverses the digit order.  The byte twins serve
+// ascending sorts only.
 template <int KT>
-__device__ __forceinline__ uint32_t digit_of(typename KeyOps<KT>::T u, uint32_t shift, uint32_t mask)
+__device__ __forceinline__ uint32_t digit_of(typename KeyOps<KT>::T u, uint32_t shift, uint32_t mask,
+                                             uint32_t flip)
 {
     if constexpr (IsByte<KT>::value)  // byte (shift / 8) moved to the low byte, zeros above
         return __byte_perm((uint32_t)KeyOps<KT>::ordered(u), 0u, 0x4440u | (shift >> 3));
     else
-        return (uint32_t)(KeyOps<KT>::ordered(u) >> shift) & mask;
+        return ((uint32_t)(KeyOps<KT>::ordered(u) >> shift) & mask) ^ flip;
 }
 
 // ------------------------------------------------------------- small helpers
@@ -189,8 +219,10 @@ __device__ __forceinline__ void st_keep(T* addr, T v, uint64_t pol)
 {
     if constexpr (sizeof(T) == 8)
         asm volatile("st.global.L2::cache_hint.b64 [%0], %1, %2;" ::"l"(addr), "l"(v), "l"(pol) : "memory");
-    else
+    else if constexpr (sizeof(T) == 4)
         asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(addr), "r"(v), "l"(pol) : "memory");
+    else
+        asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;" ::"l"(addr), "h"(v), "l"(pol) : "memory");
 }
 
 __device__ __forceinline__ uint32_t lanemask_lt()
@@ -263,6 +295,8 @@ struct PassParams {
     uint32_t n;
     uint32_t shift;          // lowest bit of this pass's digit in the ordered key
     uint32_t mask;           // digit mask (fewer bits on a final partial digit)
+    uint32_t flip;           // mask for a descending sort, else 0
+    uint32_t descending;
     uint32_t num_tiles;
     // chained scan
     uint32_t* status;        // [num_tiles][BINS] for this pass
@@ -343,24 +377,26 @@ struct SkipAcc {
     using T = typename KeyOps<KT>::T;
     T ref;          // ordered(keys[0])
     T rmask;        // bits [begin_bit, end_bit)
+    T vflip;        // for a descending sort the check runs on complemented values
     T diff = 0;
     bool unsorted = false;
 
-    __device__ __forceinline__ SkipAcc(const T* keys, uint32_t begin_bit, uint32_t end_bit)
-        : ref(KeyOps<KT>::ordered(keys[0])),
-          rmask(((end_bit - begin_bit >= 8 * sizeof(T)) ? ~T(0) : (T(1) << (end_bit - begin_bit)) - T(1))
-                << begin_bit) {}
+    __device__ __forceinline__ SkipAcc(const T* keys, uint32_t begin_bit, uint32_t end_bit, bool descending)
+        : ref((T)KeyOps<KT>::ordered(keys[0])),
+          rmask((T)((end_bit - begin_bit >= 64 ? ~0ull : (1ull << (end_bit - begin_bit)) - 1ull) << begin_bit)),
+          vflip(descending ? (MASKED ? rmask : (T)~0ull) : T(0)) {}
 
     // Folds one key into diff and returns its value for the order check.
     __device__ __forceinline__ T visit(T k)
     {
-        const T o = KeyOps<KT>::ordered(k);
+        const T o = (T)KeyOps<KT>::ordered(k);
         diff |= o ^ ref;
-        return MASKED ? (o & rmask) : o;
+        return MASKED ? (T)((o & rmask) ^ vflip) : (T)(o ^ vflip);
     }
     __device__ __forceinline__ T value(T k) const
     {
-        return MASKED ? (KeyOps<KT>::ordered(k) & rmask) : KeyOps<KT>::ordered(k);
+        const T o = (T)KeyOps<KT>::ordered(k);
+        return MASKED ? (T)((o & rmask) ^ vflip) : (T)(o ^ vflip);
     }
     __device__ __forceinline__ void pair(T a, T b) { unsorted |= a > b; }
 
@@ -631,16 +667,17 @@ __device__ __forceinline__ uint32_t warp_peers(uint32_t v)
 // tile, lanes past the end get digit BINS, which has its own dummy counter.
 template <bool FULL, int KT, int RB, int ITEMS>
 __device__ __forceinline__ uint32_t step_digit(const typename KeyOps<KT>::T (&key)[ITEMS], int k, uint32_t seg,
-                                               uint32_t n, uint32_t shift, uint32_t mask, int lane)
+                                               uint32_t n, uint32_t shift, uint32_t mask, uint32_t flip,
+                                               int lane)
 {
-    const uint32_t d = digit_of<KT>(key[k], shift, mask);
+    const uint32_t d = digit_of<KT>(key[k], shift, mask, flip);
     return (FULL || seg + k * 32 + lane < n) ? d : (1u << RB);
 }
 
 template <bool FULL, int KT, int RB, int ITEMS, int CHAINS, int WH>
 __device__ __forceinline__ void rank_in_warp(const typename KeyOps<KT>::T (&key)[ITEMS], uint32_t seg,
-                                             uint32_t n, uint32_t shift, uint32_t mask, uint32_t* wh,
-                                             int lane, uint32_t (&rank)[(ITEMS + 1) / 2])
+                                             uint32_t n, uint32_t shift, uint32_t mask, uint32_t flip,
+                                             uint32_t* wh, int lane, uint32_t (&rank)[(ITEMS + 1) / 2])
 {
     // Part c holds steps [c*L, (c+1)*L) and counts into wh + c*WH; the parts
     // are visited interleaved (j-th step of every part, then the next j).
@@ -654,7 +691,7 @@ __device__ __forceinline__ void rank_in_warp(const typename KeyOps<KT>::T (&key)
         for (int c = 0; c < CHAINS; ++c) {
             const int k = c * L + j;
             uint32_t* cnt = wh + c * WH;
-            const uint32_t d = step_digit<FULL, KT, RB, ITEMS>(key, k, seg, n, shift, mask, lane);
+            const uint32_t d = step_digit<FULL, KT, RB, ITEMS>(key, k, seg, n, shift, mask, flip, lane);
             const uint32_t peers = warp_peers<FULL ? RB : RB + 1, RB>(d);
 #if RS_RANK_ATOMIC
             const int leader = 31 - __clz(peers);
@@ -709,7 +746,7 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
 
     // (the caller has zeroed the counters and synchronised)
     uint32_t rank[(ITEMS + 1) / 2];
-    rank_in_warp<FULL, KT, RB, ITEMS, CHAINS, WH>(key, seg, p.n, p.shift, p.mask,
+    rank_in_warp<FULL, KT, RB, ITEMS, CHAINS, WH>(key, seg, p.n, p.shift, p.mask, p.flip,
                                                   whist + warp * CHAINS * WH, lane, rank);
     __syncthreads();
 
@@ -740,7 +777,7 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
     const uint32_t* wbase = whist + warp * CHAINS * WH;
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
-        const uint32_t d = step_digit<FULL, KT, RB, ITEMS>(key, k, seg, p.n, p.shift, p.mask, lane);
+        const uint32_t d = step_digit<FULL, KT, RB, ITEMS>(key, k, seg, p.n, p.shift, p.mask, p.flip, lane);
         const uint32_t r = (k & 1) ? (rank[k / 2] >> 16) : (rank[k / 2] & 0xFFFFu);
         uint32_t pos = wbase[(k / (ITEMS / CHAINS)) * WH + d] + r;
 #if RS_CHECKED
@@ -783,7 +820,7 @@ __device__ __forceinline__ void tile_scatter(const PassParams& p, unsigned char*
         const uint32_t s = (uint32_t)(k * THREADS) + threadIdx.x;
         if (FULL || s < valid) {
             const T kk = skeys[s];
-            const uint32_t idx = sbase[digit_of<KT>(kk, p.shift, p.mask)] + s;
+            const uint32_t idx = sbase[digit_of<KT>(kk, p.shift, p.mask, p.flip)] + s;
             const bool ok = idx < p.n;
             bad |= !ok;
             if (ok) {
@@ -993,8 +1030,8 @@ __global__ void __launch_bounds__(THREADS) k_upsweep(PassParams p)
     const uint64_t hi64 = lo64 + (uint64_t)p.tiles_per_cta * TILE;
     const uint32_t hi = hi64 < p.n ? (uint32_t)hi64 : p.n;
     const T* src = static_cast<const T*>(p.keys_in);
-    auto count = [&](T k) { atomicAdd(&hist[digit_of<KT>(k, p.shift, p.mask) * COLS + col], 1u); };
-    SkipAcc<KT> acc(src, p.begin_bit, p.end_bit);
+    auto count = [&](T k) { atomicAdd(&hist[digit_of<KT>(k, p.shift, p.mask, p.flip) * COLS + col], 1u); };
+    SkipAcc<KT> acc(src, p.begin_bit, p.end_bit, p.descending != 0u);
     // lo is a multiple of TILE, so lo * sizeof(T) is 16-byte aligned whenever the base is.
     uint32_t i = lo;
     if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
@@ -1220,6 +1257,7 @@ struct ClusterParams {
     uint32_t end_bit;
     uint32_t* err;
     uint32_t* skip;   // the skip record, for rs_skip_record
+    uint32_t descending;
 };
 
 template <typename T, int RB, int THREADS, int ITEMS, bool VALS>
@@ -1281,7 +1319,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_cluster_sort(ClusterParams cp)
     if (tid < 4) rec[tid] = 0u;
     __syncthreads();
     {
-        SkipAcc<KT> acc(gin, cp.begin_bit, cp.end_bit);
+        SkipAcc<KT> acc(gin, cp.begin_bit, cp.end_bit, cp.descending != 0u);
         T v[ITEMS];
 #pragma unroll
         for (int k = 0; k < ITEMS; ++k) {
@@ -1347,6 +1385,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_cluster_sort(ClusterParams cp)
         }
         p.shift = cp.begin_bit + q * RB;
         p.mask = (1u << min((uint32_t)RB, cp.end_bit - p.shift)) - 1u;
+        p.flip = cp.descending ? p.mask : 0u;
         zero_counters<S>(smem, THREADS);
         __syncthreads();
         uint32_t cnt, start;
@@ -1379,7 +1418,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_cluster_sort(ClusterParams cp)
             const uint32_t s = (uint32_t)(k * THREADS) + tid;
             if (s < valid) {
                 const T kk = skeys[s];
-                const uint32_t g = sbase[digit_of<KT>(kk, p.shift, p.mask)] + s;
+                const uint32_t g = sbase[digit_of<KT>(kk, p.shift, p.mask, p.flip)] + s;
                 if (g >= cp.n) {
                     bad = 1;
                     continue;
@@ -1419,6 +1458,7 @@ struct HistParams {
     int aligned16;          // keys pointer is 16-byte aligned
     uint32_t* skip;         // the pass-skip record
     uint32_t* plan;         // the pass plan
+    uint32_t descending;
 };
 
 // Counters are lane-private columns, hist[pass][bin][col] with col = lane %
@@ -1448,7 +1488,8 @@ __global__ void __launch_bounds__(THREADS) k_histogram(HistParams h)
         uint32_t* row = hist + col;
         for (uint32_t q = 0; q < h.passes; ++q, shift += RB, row += BINS * COLS) {
             const uint32_t width = min((uint32_t)RB, h.end_bit - shift);
-            const uint32_t d = (uint32_t)(o >> shift) & ((1u << width) - 1u);
+            const uint32_t m = (1u << width) - 1u;
+            const uint32_t d = ((uint32_t)(o >> shift) & m) ^ (h.descending ? m : 0u);
             atomicAdd(row + d * COLS, 1u);
         }
     };
@@ -1457,7 +1498,7 @@ __global__ void __launch_bounds__(THREADS) k_histogram(HistParams h)
     const size_t gid = (size_t)blockIdx.x * THREADS + tid;
     const int lane = tid & 31;
     const T* keys = static_cast<const T*>(h.keys);
-    SkipAcc<KT, !FULLRANGE> acc(keys, h.begin_bit, h.end_bit);
+    SkipAcc<KT, !FULLRANGE> acc(keys, h.begin_bit, h.end_bit, h.descending != 0u);
     size_t done = 0;
     if (h.aligned16) {
         const size_t nvec = h.n / VEC;
@@ -1529,6 +1570,7 @@ struct Plan {
     int begin_bit, end_bit;
     int algo;         // RS_ALGO_ONESWEEP or RS_ALGO_REDUCE_SCAN (resolved)
     int radix_bits;   // 4 or 8
+    bool descending;
     int passes;
     const void* keys_in;
     void* keys_out;
@@ -1592,6 +1634,9 @@ template <int KT> struct ByteTwin { static constexpr int value = KT; };
 template <> struct ByteTwin<KU32> { static constexpr int value = KU32B; };
 template <> struct ByteTwin<KI32> { static constexpr int value = KI32B; };
 template <> struct ByteTwin<KF32> { static constexpr int value = KF32B; };
+template <> struct ByteTwin<KU16> { static constexpr int value = KU16B; };
+template <> struct ByteTwin<KI16> { static constexpr int value = KI16B; };
+template <> struct ByteTwin<KF16> { static constexpr int value = KF16B; };
 
 template <int KT, int RB, bool VALS>
 rs_status run_passes(Plan& pl)
@@ -1624,6 +1669,7 @@ rs_status run_passes(Plan& pl)
     base.begin_bit = (uint32_t)pl.begin_bit;
     base.end_bit = (uint32_t)pl.end_bit;
     base.in_place = in_place ? 1u : 0u;
+    base.descending = pl.descending ? 1u : 0u;
     base.n = n;
     base.err = meta + kErrWord;
     base.spin_limit = pl.spin_limit;
@@ -1672,6 +1718,7 @@ rs_status run_passes(Plan& pl)
         h.zero = reinterpret_cast<uint4*>(big);
         h.zero_vec4 = status_words / 4;
         h.aligned16 = (reinterpret_cast<uintptr_t>(pl.keys_in) % 16) == 0;
+        h.descending = pl.descending ? 1u : 0u;
         h.skip = meta + kSkipBase;
         h.plan = meta + kPlanBase;
         const size_t want = (n + 1024 * 16 - 1) / (1024 * 16);
@@ -1688,10 +1735,12 @@ rs_status run_passes(Plan& pl)
             pp.shift = pl.begin_bit + q * RB;
             const uint32_t width = std::min(RB, pl.end_bit - (int)pp.shift);
             pp.mask = (1u << width) - 1u;
+        pp.flip = pl.descending ? pp.mask : 0u;
+            pp.flip = pl.descending ? pp.mask : 0u;
             pp.status = big + (size_t)q * num_tiles * BINS;
             pp.ghist = meta + kGhistBase + q * BINS;
             pp.ticket = meta + kTicketBase + q;
-            const bool byte_digit = (RB == 8) && (pp.shift % 8 == 0) && (pp.mask == 0xFFu);
+            const bool byte_digit = (RB == 8) && (pp.shift % 8 == 0) && (pp.mask == 0xFFu) && !pl.descending;
             if (!pl.count_only) (byte_digit ? pkb : pk)<<<num_tiles, THREADS, S::bytes, pl.stream>>>(pp);
             st = after_launch(pl, kKindOnesweep);
             if (st != RS_OK) return st;
@@ -1727,6 +1776,7 @@ rs_status run_passes(Plan& pl)
         pp.shift = pl.begin_bit + q * RB;
         const uint32_t width = std::min(RB, pl.end_bit - (int)pp.shift);
         pp.mask = (1u << width) - 1u;
+        pp.flip = pl.descending ? pp.mask : 0u;
         pp.counts = big;
         pp.G = G;
         pp.tiles_per_cta = tpc;
@@ -1737,7 +1787,7 @@ rs_status run_passes(Plan& pl)
         if (!pl.count_only) k_spine_scan<RB, 256><<<BINS, 256, 0, pl.stream>>>(pp, meta + kGhistBase + q * BINS);
         st = after_launch(pl, kKindSpine);
         if (st != RS_OK) return st;
-        const bool byte_digit = (RB == 8) && (pp.shift % 8 == 0) && (pp.mask == 0xFFu);
+        const bool byte_digit = (RB == 8) && (pp.shift % 8 == 0) && (pp.mask == 0xFFu) && !pl.descending;
         if (!pl.count_only) (byte_digit ? dkb : dk)<<<G, THREADS, S::bytes, pl.stream>>>(pp);
         st = after_launch(pl, kKindDownsweep);
         if (st != RS_OK) return st;
@@ -1821,6 +1871,7 @@ rs_status run_cluster(Plan& pl)
     cp.passes = (uint32_t)pl.passes;
     cp.begin_bit = (uint32_t)pl.begin_bit;
     cp.end_bit = (uint32_t)pl.end_bit;
+    cp.descending = pl.descending ? 1u : 0u;
     cp.err = meta + kErrWord;
     cp.skip = meta + kSkipBase;
     cudaLaunchConfig_t cfg = {};

@@ -1,0 +1,7 @@
+// rs_sort_f16.cu -- instantiates the sort kernels and driver for one key type
+// (kept in its own translation unit so the key types compile in parallel).
+#include "rs_kernels.cuh"
+
+namespace rs {
+template rs_status run_sort<KF16>(Plan& pl);
+}  // namespace rs

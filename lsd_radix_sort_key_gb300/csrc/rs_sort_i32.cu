@@ -1,5 +1,5 @@
 // rs_sort_i32.cu -- instantiates the sort kernels and driver for one key type
-// (kept in its own translation unit so the four compile in parallel).
+// (kept in its own translation unit so the key types compile in parallel).
 #include "rs_kernels.cuh"
 
 namespace rs {

@@ -4,19 +4,22 @@ import numpy as np
 
 import lsd_radix_sort_key_gb300 as rs
 
-NP_KEY = {"u32": np.uint32, "i32": np.uint32, "f32": np.uint32, "u64": np.uint64}
+NP_KEY = {"u32": np.uint32, "i32": np.uint32, "f32": np.uint32, "u64": np.uint64,
+          "u16": np.uint16, "i16": np.uint16, "f16": np.uint16}
+_VIEW = {8: np.int64, 4: np.int32, 2: np.int16}
 
 
 def to_dev(a, dev):
     import torch
     if a is None:
         return None
-    view = a.view(np.int64) if a.dtype.itemsize == 8 else a.view(np.int32)
+    view = a.view(_VIEW[a.dtype.itemsize])
     return torch.from_numpy(np.ascontiguousarray(view)).to(dev)
 
 
 def gpu_sort(kt, keys, vals=None, begin_bit=0, end_bit=None, algo="auto", radix_bits=0,
-             dev="cuda:0", offset=0, in_place=False, check_status=True, want_record=False):
+             dev="cuda:0", offset=0, in_place=False, check_status=True, want_record=False,
+             descending=False):
     """Sort on the GPU via rs_sort; `offset` elements of padding before the
     input exercise unaligned pointers.  Returns (keys, vals) as numpy, plus
     the pass-skip record (differing_bits, unordered) if want_record."""
@@ -40,7 +43,7 @@ def gpu_sort(kt, keys, vals=None, begin_bit=0, end_bit=None, algo="auto", radix_
     temp = torch.empty(max(tb, 256), dtype=torch.uint8, device=dev)
     d = rs.make_desc(kt, kin if n else None, kout if n else None, vin if n else None,
                      vout if n else None, n, begin_bit, end_bit, temp, temp.numel(),
-                     None, algo, radix_bits)
+                     None, algo, radix_bits, descending=descending)
     st = rs.rs_sort(d)
     assert st == 0, rs.STATUS.get(st, st)
     torch.cuda.synchronize()

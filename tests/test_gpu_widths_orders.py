@@ -1,0 +1,125 @@
+"""16-bit keys and descending order, bit-exact against the CPU oracle (needs a GPU).
+
+uint16, int16 and binary16 keys under every schedule and both digit widths,
+with and without values, full and partial bit ranges, in place, unaligned
+and through the typed entry points; descending order for every key type,
+including the inputs that skip passes (already in ascending order: nothing
+skipped; already in descending order: every pass skipped), whose skip record
+is checked against its definition.
+"""
+import numpy as np
+import pytest
+
+import lsd_radix_sort_key_gb300 as rs
+import oracle
+import synth
+from gpu_util import gpu_sort, to_dev
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    rs.build()
+    rs.lib()
+
+
+ALGOS = ["onesweep", "reduce_scan", "cluster"]
+
+
+def gen_keys(kt, n, seed):
+    if kt == "u64":
+        return synth.u64_uniform(n, seed)
+    if kt == "f32":
+        return synth.f32_edge(n, seed)
+    if kt == "f16":
+        return synth.f16_edge(n, seed)
+    if kt in ("u16", "i16"):
+        return synth.u16_uniform(n, seed)
+    return synth.u32_uniform(n, seed)
+
+
+def check(kt, keys, vals, b, e, descending=False, **kw):
+    got_k, got_v = gpu_sort(kt, keys, vals, b, e, descending=descending, **kw)
+    ref_k, ref_v = oracle.sort(kt, keys, vals, b, e, descending=descending)
+    assert np.array_equal(got_k, ref_k), f"keys differ ({kt}, n={len(keys)}, [{b},{e}), {kw})"
+    if vals is not None:
+        assert np.array_equal(got_v, ref_v), f"values differ ({kt}, n={len(keys)}, [{b},{e}), {kw})"
+
+
+def sizes(algo, kt, with_vals):
+    if algo == "cluster":
+        cap = rs.rs_cluster_max_n(kt, with_vals)
+        return [1, 31, 3841, cap // 2 + 1, cap]
+    return [1, 31, 3841, 50_000, 300_001]
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("kt", ["u16", "i16", "f16"])
+@pytest.mark.parametrize("with_vals", [False, True])
+@pytest.mark.parametrize("radix_bits", [8, 4])
+def test_16bit_keys(algo, kt, with_vals, radix_bits):
+    for i, n in enumerate(sizes(algo, kt, with_vals)):
+        keys = gen_keys(kt, n, 900 + i)
+        vals = synth.iota_u32(n) if with_vals else None
+        check(kt, keys, vals, 0, 16, algo=algo, radix_bits=radix_bits)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_16bit_ranges_in_place_unaligned(algo):
+    n = sizes(algo, "u16", True)[-1]
+    keys = synth.u16_uniform(n, 950)
+    for b, e in [(0, 5), (3, 14), (8, 16), (4, 12)]:
+        check("u16", keys, synth.iota_u32(n), b, e, algo=algo)
+    check("f16", synth.f16_normal_specials(n, 951), synth.iota_u32(n), 0, 16, algo=algo, in_place=True)
+    check("i16", keys, None, 0, 16, algo=algo, offset=1)
+    check("u16", keys & np.uint16(0xFF), synth.iota_u32(n), 0, 16, algo=algo)     # high pass skipped
+
+
+def test_16bit_typed_entry_points():
+    n = 70_001
+    keys = synth.f16_normal_specials(n, 960)
+    kin = to_dev(keys, "cuda:0")
+    kout = torch.empty_like(kin)
+    vin = to_dev(synth.iota_u32(n), "cuda:0")
+    vout = torch.empty_like(vin)
+    tb = rs.rs_temp_bytes("f16", True, n, 0, 16)
+    temp = torch.empty(tb, dtype=torch.uint8, device="cuda:0")
+    assert rs.rs_sort_pairs_f16(kin, kout, vin, vout, n, 0, 16, temp, tb, None) == 0
+    torch.cuda.synchronize()
+    ref_k, ref_v = oracle.sort("f16", keys, synth.iota_u32(n), 0, 16)
+    assert np.array_equal(kout.cpu().numpy().view(np.uint16), ref_k)
+    assert np.array_equal(vout.cpu().numpy().view(np.uint32), ref_v)
+    assert rs.rs_sort_keys_u16(kin, kout, n, 0, 16, temp, tb, None) == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(kout.cpu().numpy().view(np.uint16), oracle.sort("u16", keys)[0])
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("kt", ["u32", "i32", "f32", "u64", "u16", "f16"])
+@pytest.mark.parametrize("with_vals", [False, True])
+def test_descending(algo, kt, with_vals):
+    for i, n in enumerate(sizes(algo, kt, with_vals)):
+        keys = gen_keys(kt, n, 1000 + i)
+        vals = synth.iota_u32(n) if with_vals else None
+        check(kt, keys, vals, 0, rs.KEY_BITS[kt], descending=True, algo=algo)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_descending_partial_ranges_ties_and_skips(algo):
+    n = sizes(algo, "u32", True)[-1]
+    keys = synth.u32_uniform(n, 1100)
+    vals = synth.iota_u32(n)
+    check("u32", keys, vals, 5, 27, descending=True, algo=algo, radix_bits=4)
+    check("u32", synth.u32_bits(n, 1101, 3), vals, 0, 32, descending=True, algo=algo)     # ties
+    check("u32", keys, vals, 0, 32, descending=True, algo=algo, in_place=True)
+    up = oracle.sort("u32", keys, None, 0, 32)[0]
+    down = oracle.sort("u32", keys, None, 0, 32, descending=True)[0]
+    for inp, unordered in ((up, 1), (down, 0)):
+        got, _, rec = gpu_sort("u32", inp, None, 0, 32, algo=algo, descending=True, want_record=True)
+        assert np.array_equal(got, down)
+        assert rec[1] == unordered
