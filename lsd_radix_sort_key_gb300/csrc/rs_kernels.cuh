@@ -1001,9 +1001,10 @@ __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS)
 // digit-major (counts[d * G + g]) so that one exclusive scan of the whole
 // array yields every (digit, CTA) start ("Radix sort paralelo sobre el scan",
 // section "Las tres fases de una pasada").
-// The first upsweep (FIRST) also writes the pass-skip record; every later one
-// runs only if its pass does.
-template <int KT, int RB, int THREADS, int TILE, bool FIRST>
+// The first upsweep (FIRST) also writes the pass-skip record (FULLRANGE: the
+// sorted bits are the whole key, so its order check needs no mask); every
+// later one runs only if its pass does.
+template <int KT, int RB, int THREADS, int TILE, bool FIRST, bool FULLRANGE = false>
 __global__ void __launch_bounds__(THREADS) k_upsweep(PassParams p)
 {
     using T = typename KeyOps<KT>::T;
@@ -1031,7 +1032,7 @@ __global__ void __launch_bounds__(THREADS) k_upsweep(PassParams p)
     const uint32_t hi = hi64 < p.n ? (uint32_t)hi64 : p.n;
     const T* src = static_cast<const T*>(p.keys_in);
     auto count = [&](T k) { atomicAdd(&hist[digit_of<KT>(k, p.shift, p.mask, p.flip) * COLS + col], 1u); };
-    SkipAcc<KT> acc(src, p.begin_bit, p.end_bit, p.descending != 0u);
+    SkipAcc<KT, !FULLRANGE> acc(src, p.begin_bit, p.end_bit, p.descending != 0u);
     // lo is a multiple of TILE, so lo * sizeof(T) is 16-byte aligned whenever the base is.
     uint32_t i = lo;
     if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
@@ -1093,7 +1094,9 @@ __global__ void __launch_bounds__(THREADS) k_upsweep(PassParams p)
         acc.flush_warp(skip_blk);
     }
     __syncthreads();
-    if constexpr (FIRST) SkipAcc<KT>::template flush_block<RB>(skip_blk, p.skip, p.plan, p.passes, p.begin_bit, p.end_bit);
+    if constexpr (FIRST)
+        SkipAcc<KT, !FULLRANGE>::template flush_block<RB>(skip_blk, p.skip, p.plan, p.passes, p.begin_bit,
+                                                          p.end_bit);
     for (int d = tid; d < BINS; d += THREADS) {
         uint32_t c = 0;
 #pragma unroll 8
@@ -1482,15 +1485,25 @@ __global__ void __launch_bounds__(THREADS) k_histogram(HistParams h)
     if (tid < 3) skip_blk[tid] = 0;
     __syncthreads();
 
+    // Each pass's shift, digit mask and flip, worked out once; the key loop
+    // below is unrolled over the most passes this key type can have.
+    constexpr int MAXP = (8 * (int)sizeof(T) + RB - 1) / RB;
+    uint32_t sh[MAXP], mk[MAXP], fl[MAXP];
+#pragma unroll
+    for (int q = 0; q < MAXP; ++q) {
+        sh[q] = min(h.begin_bit + q * RB, 8u * (uint32_t)sizeof(T) - 1u);
+        const uint32_t width = (uint32_t)q < h.passes ? min((uint32_t)RB, h.end_bit - sh[q]) : 0u;
+        mk[q] = (1u << width) - 1u;
+        fl[q] = h.descending ? mk[q] : 0u;
+    }
     auto count = [&](T k) {
         const auto o = KeyOps<KT>::ordered(k);
-        uint32_t shift = h.begin_bit;
-        uint32_t* row = hist + col;
-        for (uint32_t q = 0; q < h.passes; ++q, shift += RB, row += BINS * COLS) {
-            const uint32_t width = min((uint32_t)RB, h.end_bit - shift);
-            const uint32_t m = (1u << width) - 1u;
-            const uint32_t d = ((uint32_t)(o >> shift) & m) ^ (h.descending ? m : 0u);
-            atomicAdd(row + d * COLS, 1u);
+#pragma unroll
+        for (int q = 0; q < MAXP; ++q) {
+            if ((uint32_t)q < h.passes) {
+                const uint32_t d = ((uint32_t)(o >> sh[q]) & mk[q]) ^ fl[q];
+                atomicAdd(hist + (q * BINS + d) * COLS + col, 1u);
+            }
         }
     };
 
@@ -1754,7 +1767,8 @@ rs_status run_passes(Plan& pl)
     using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
     const uint32_t num_tiles = (n + TILE - 1) / TILE;
     base.num_tiles = num_tiles;
-    auto uk0 = k_upsweep<KT, RB, 512, TILE, true>;
+    const bool full_range = pl.begin_bit == 0 && pl.end_bit == 8 * KB;
+    auto uk0 = full_range ? k_upsweep<KT, RB, 512, TILE, true, true> : k_upsweep<KT, RB, 512, TILE, true, false>;
     auto uk = k_upsweep<KT, RB, 512, TILE, false>;
     auto dk = k_downsweep<KT, RB, THREADS, ITEMS, VALS>;
     auto dkb = k_downsweep<ByteTwin<KT>::value, RB, THREADS, ITEMS, VALS>;
