@@ -108,6 +108,7 @@ typedef enum rs_algo {
 /*
  * Bytes of device scratch ("temp") a sort of this shape needs, for every
  * schedule and digit width, so one temp buffer serves any rs_sort variant.
+ * with_values: 0 keys only, 8 uint64 values, any other value uint32 values.
  * Pure host arithmetic: needs no GPU and never fails (0 for n == 0).
  * Returns (size_t)-1 for arguments every sort would reject.
  */
@@ -163,8 +164,8 @@ typedef struct rs_sort_desc {
     rs_key_type key_type;
     const void* keys_in;
     void* keys_out;
-    const uint32_t* vals_in;
-    uint32_t* vals_out;
+    const void* vals_in;   /* n values of value_bytes each, or NULL (keys only) */
+    void* vals_out;
     size_t n;
     int begin_bit;
     int end_bit;
@@ -181,6 +182,9 @@ typedef struct rs_sort_desc {
     int32_t stall_tile;
     /* 1: descending order of D (ties still in input order); 0: ascending. */
     int descending;
+    /* Bytes per value: 0 or 4 = uint32 values, 8 = uint64 values (ignored
+     * for keys only); value pointers must be aligned to it. */
+    int value_bytes;
 } rs_sort_desc;
 
 rs_status rs_sort(const rs_sort_desc* desc);
@@ -203,8 +207,9 @@ rs_status rs_sort_profiled(const rs_sort_desc* desc, void* const* events, int ma
 
 /*
  * Largest n the cluster schedule (RS_ALGO_CLUSTER) sorts: 16 CTAs x one tile
- * each -- 65536 uint32/int32/float keys, 49152 of them with values or uint64
- * keys, 32768 uint64 keys with values.  Up to half of that runs on 8 CTAs
+ * each -- 65536 32- or 16-bit keys, 49152 of them with uint32 values or
+ * uint64 keys, 32768 with uint64 values or uint64 keys with uint32 values,
+ * 24576 uint64 keys with uint64 values (with_values as for rs_temp_bytes).  Up to half of that runs on 8 CTAs
  * (the portable cluster size); above it the cluster needs 16, which a device
  * may not schedule: then RS_ALGO_CLUSTER returns RS_ERR_UNSUPPORTED and AUTO
  * takes the chained scan.  No CUDA call; 0 for an invalid key type.

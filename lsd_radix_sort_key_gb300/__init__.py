@@ -44,7 +44,7 @@ class SortDesc(ctypes.Structure):
                 ("radix_bits", ctypes.c_int), ("temp", ctypes.c_void_p),
                 ("temp_bytes", ctypes.c_size_t), ("stream", ctypes.c_void_p),
                 ("spin_limit", ctypes.c_uint32), ("stall_tile", ctypes.c_int32),
-                ("descending", ctypes.c_int)]
+                ("descending", ctypes.c_int), ("value_bytes", ctypes.c_int)]
 
 
 _lib = None
@@ -120,8 +120,14 @@ def _check(code: int, where: str):
 
 # ---------------------------------------------------------- C-named wrappers
 
-def rs_temp_bytes(key_type: str, with_values: bool, n: int, begin_bit: int, end_bit: int) -> int:
-    return lib().rs_temp_bytes(KEY_TYPES[key_type], int(bool(with_values)), n, begin_bit, end_bit)
+def _with_values(v) -> int:
+    """C with_values argument: False/0 none, 8 uint64 values, True/4 uint32 values."""
+    return 8 if (v is not True and v == 8) else int(bool(v))
+
+
+def rs_temp_bytes(key_type: str, with_values, n: int, begin_bit: int, end_bit: int) -> int:
+    """with_values: False, True (uint32 values) or 8 (uint64 values)."""
+    return lib().rs_temp_bytes(KEY_TYPES[key_type], _with_values(with_values), n, begin_bit, end_bit)
 
 
 def rs_host_work_bytes(key_type: str, with_values: bool, n: int, begin_bit: int, end_bit: int) -> int:
@@ -167,10 +173,11 @@ def rs_sort_keys_u32_noalloc(keys_in, keys_out, n, begin_bit, end_bit, stream=No
 
 def make_desc(key_type, keys_in, keys_out, vals_in, vals_out, n, begin_bit, end_bit, temp,
               temp_bytes, stream=None, algo="auto", radix_bits=0, spin_limit=0, stall_tile=0,
-              descending=False):
+              descending=False, value_bytes=0):
     return SortDesc(KEY_TYPES[key_type], _addr(keys_in), _addr(keys_out), _addr(vals_in),
                     _addr(vals_out), n, begin_bit, end_bit, ALGOS[algo], radix_bits, _addr(temp),
-                    temp_bytes, _stream(stream), spin_limit, stall_tile, int(bool(descending)))
+                    temp_bytes, _stream(stream), spin_limit, stall_tile, int(bool(descending)),
+                    value_bytes)
 
 
 def rs_sort(desc: SortDesc) -> int:
@@ -198,9 +205,9 @@ def rs_device_status(temp, stream=None) -> int:
     return lib().rs_device_status(_addr(temp), _stream(stream))
 
 
-def rs_cluster_max_n(key_type: str, with_values: bool) -> int:
-    """Largest n the one-kernel cluster schedule sorts."""
-    return lib().rs_cluster_max_n(KEY_TYPES[key_type], int(bool(with_values)))
+def rs_cluster_max_n(key_type: str, with_values) -> int:
+    """Largest n the one-kernel cluster schedule sorts (with_values as for rs_temp_bytes)."""
+    return lib().rs_cluster_max_n(KEY_TYPES[key_type], _with_values(with_values))
 
 
 def rs_skip_record(temp, stream=None):
@@ -256,7 +263,7 @@ def key_type_of(t) -> str:
 
 def sort(keys, values=None, *, key_type=None, begin_bit=0, end_bit=None, algo="auto",
          radix_bits=0, keys_out=None, values_out=None, temp=None, stream=None, descending=False):
-    """Stable radix sort of a CUDA tensor of keys (and uint32 values),
+    """Stable radix sort of a CUDA tensor of keys (and 32- or 64-bit values),
     ascending or descending (ties keep their input order either way).
 
     Returns (keys_out, values_out or None).  Allocates the outputs and temp
@@ -273,12 +280,15 @@ def sort(keys, values=None, *, key_type=None, begin_bit=0, end_bit=None, algo="a
         keys_out = torch.empty_like(keys)
     if values is not None and values_out is None:
         values_out = torch.empty_like(values)
-    tb = rs_temp_bytes(kt, values is not None, n, begin_bit, end_bit)
+    vb = 0 if values is None else values.element_size()
+    if vb not in (0, 4, 8):
+        raise ValueError("values must have 4- or 8-byte elements")
+    tb = rs_temp_bytes(kt, vb if vb else False, n, begin_bit, end_bit)
     if tb == ctypes.c_size_t(-1).value:
         raise RadixSortError(1, "rs_temp_bytes")
     if temp is None:
         temp = torch.empty(max(tb, 1), dtype=torch.uint8, device=keys.device)
     desc = make_desc(kt, keys, keys_out, values, values_out, n, begin_bit, end_bit, temp,
-                     temp.numel(), stream, algo, radix_bits, descending=descending)
+                     temp.numel(), stream, algo, radix_bits, descending=descending, value_bytes=vb)
     _check(rs_sort(desc), "rs_sort")
     return keys_out, values_out

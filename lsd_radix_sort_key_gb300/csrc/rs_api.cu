@@ -32,6 +32,8 @@ constexpr uint32_t kDefaultSpinLimit = 1u << 20;      // each spin is one L2 rou
 int key_bytes(rs_key_type kt) { return kt == RS_U64 ? 8 : kt >= RS_U16 ? 2 : 4; }
 int key_bits(rs_key_type kt) { return 8 * key_bytes(kt); }
 bool valid_kt(int kt) { return kt >= RS_U32 && kt <= RS_F16; }
+// rs_temp_bytes / rs_cluster_max_n take with_values: 0 none, 8 uint64, else uint32.
+int value_bytes_of(int with_values) { return with_values == 0 ? 0 : with_values == 8 ? 8 : 4; }
 
 bool ranges_overlap(const void* a, size_t abytes, const void* b, size_t bbytes)
 {
@@ -56,6 +58,8 @@ rs_status make_plan(const rs_sort_desc* d, rs::Plan* pl)
     if (st != RS_OK) return st;
     const bool vals = d->vals_in != nullptr || d->vals_out != nullptr;
     if (vals && (!d->vals_in || !d->vals_out)) return RS_ERR_INVALID_ARG;
+    if (d->value_bytes != 0 && d->value_bytes != 4 && d->value_bytes != 8) return RS_ERR_INVALID_ARG;
+    const int vb = vals ? (d->value_bytes == 8 ? 8 : 4) : 0;
     if (d->radix_bits != 0 && d->radix_bits != 4 && d->radix_bits != 8) return RS_ERR_INVALID_ARG;
     if (d->algo != RS_ALGO_AUTO && d->algo != RS_ALGO_ONESWEEP && d->algo != RS_ALGO_REDUCE_SCAN &&
         d->algo != RS_ALGO_CLUSTER)
@@ -67,6 +71,7 @@ rs_status make_plan(const rs_sort_desc* d, rs::Plan* pl)
     *pl = rs::Plan{};
     pl->kt = d->key_type;
     pl->vals = vals;
+    pl->vb = vb;
     pl->n = n;
     pl->begin_bit = d->begin_bit;
     pl->end_bit = d->end_bit;
@@ -74,7 +79,7 @@ rs_status make_plan(const rs_sort_desc* d, rs::Plan* pl)
     pl->descending = d->descending != 0;
     pl->passes = rs::passes_for(d->begin_bit, d->end_bit, pl->radix_bits);
     pl->algo = d->algo;
-    const size_t cluster_max = rs::cluster_max_n(kb, vals);
+    const size_t cluster_max = rs::cluster_max_n(kb, vb);
     if (pl->algo == RS_ALGO_AUTO) {
         // Chosen by measurement on GB300: one cluster kernel while the keys fit
         // in 8 CTAs' shared memory; reduce-then-scan from 2^25 keys for every
@@ -98,13 +103,13 @@ rs_status make_plan(const rs_sort_desc* d, rs::Plan* pl)
 
     if (!d->keys_in || !d->keys_out || !d->temp) return RS_ERR_INVALID_ARG;
     if ((uintptr_t)d->keys_in % kb || (uintptr_t)d->keys_out % kb) return RS_ERR_INVALID_ARG;
-    if (vals && ((uintptr_t)d->vals_in % 4 || (uintptr_t)d->vals_out % 4)) return RS_ERR_INVALID_ARG;
+    if (vals && ((uintptr_t)d->vals_in % vb || (uintptr_t)d->vals_out % vb)) return RS_ERR_INVALID_ARG;
     if ((uintptr_t)d->temp % 256) return RS_ERR_INVALID_ARG;
-    pl->lay = rs::temp_layout(kb, vals, n, d->begin_bit, d->end_bit);
+    pl->lay = rs::temp_layout(kb, vb, n, d->begin_bit, d->end_bit);
     if (d->temp_bytes < pl->lay.total) return RS_ERR_TEMP_TOO_SMALL;
 
     // Aliasing: exact in-place is allowed; any other overlap is rejected.
-    const size_t kbytes = n * kb, vbytes = n * 4;
+    const size_t kbytes = n * kb, vbytes = n * (size_t)vb;
     const void* bufs[5] = {d->keys_in, d->keys_out, d->vals_in, d->vals_out, d->temp};
     const size_t sizes[5] = {kbytes, kbytes, vals ? vbytes : 0, vals ? vbytes : 0, pl->lay.total};
     for (int i = 0; i < 5; ++i)
@@ -147,7 +152,7 @@ rs_status enqueue(rs::Plan& pl)
                             cudaMemcpyDeviceToDevice, pl.stream) != cudaSuccess)
             return RS_ERR_CUDA;
         if (pl.vals && pl.vals_out != pl.vals_in &&
-            cudaMemcpyAsync(pl.vals_out, pl.vals_in, pl.n * 4, cudaMemcpyDeviceToDevice, pl.stream) !=
+            cudaMemcpyAsync(pl.vals_out, pl.vals_in, pl.n * (size_t)pl.vb, cudaMemcpyDeviceToDevice, pl.stream) !=
                 cudaSuccess)
             return RS_ERR_CUDA;
         return cudaGetLastError() == cudaSuccess ? RS_OK : RS_ERR_CUDA;
@@ -163,7 +168,7 @@ size_t rs_temp_bytes(rs_key_type key_type, int with_values, size_t n, int begin_
 {
     if (check_shape(key_type, n, begin_bit, end_bit) != RS_OK) return (size_t)-1;
     if (n == 0) return 0;
-    return rs::temp_layout(key_bytes(key_type), with_values != 0, n, begin_bit, end_bit).total;
+    return rs::temp_layout(key_bytes(key_type), value_bytes_of(with_values), n, begin_bit, end_bit).total;
 }
 
 rs_status rs_sort(const rs_sort_desc* desc)
@@ -183,8 +188,8 @@ int rs_sort_kernel_count(const rs_sort_desc* desc)
     const bool vals = d.vals_in || d.vals_out;
     if (!d.keys_in) d.keys_in = reinterpret_cast<const void*>((uintptr_t)1 << 40);
     if (!d.keys_out) d.keys_out = reinterpret_cast<void*>((uintptr_t)2 << 40);
-    if (vals && !d.vals_in) d.vals_in = reinterpret_cast<const uint32_t*>((uintptr_t)3 << 40);
-    if (vals && !d.vals_out) d.vals_out = reinterpret_cast<uint32_t*>((uintptr_t)4 << 40);
+    if (vals && !d.vals_in) d.vals_in = reinterpret_cast<const void*>((uintptr_t)3 << 40);
+    if (vals && !d.vals_out) d.vals_out = reinterpret_cast<void*>((uintptr_t)4 << 40);
     if (!d.temp) {
         d.temp = reinterpret_cast<void*>((uintptr_t)5 << 40);
         d.temp_bytes = (size_t)1 << 40;
@@ -283,7 +288,7 @@ rs_status rs_device_status(const void* temp, void* stream)
 size_t rs_cluster_max_n(rs_key_type key_type, int with_values)
 {
     if (!valid_kt(key_type)) return 0;
-    return rs::cluster_max_n(key_bytes(key_type), with_values != 0);
+    return rs::cluster_max_n(key_bytes(key_type), value_bytes_of(with_values));
 }
 
 rs_status rs_skip_record(const void* temp, void* stream, uint64_t* differing_bits, int* unordered)
@@ -374,7 +379,7 @@ void rs_graph_destroy(rs_graph* graph)
 static rs::TempLayout host_work_layout(rs_key_type kt, bool vals, size_t n, int begin_bit, int end_bit,
                                        size_t* kin, size_t* kout, size_t* vin, size_t* vout)
 {
-    rs::TempLayout t = rs::temp_layout(key_bytes(kt), vals, n, begin_bit, end_bit);
+    rs::TempLayout t = rs::temp_layout(key_bytes(kt), vals ? 4 : 0, n, begin_bit, end_bit);
     size_t off = t.total;
     const size_t kb = rs::align_up(n * key_bytes(kt), 256), vb = vals ? rs::align_up(n * 4, 256) : 0;
     *kin = off; off += kb;
@@ -416,13 +421,13 @@ rs_status rs_sort_host(rs_key_type key_type, const void* h_keys_in, void* h_keys
     d.key_type = key_type;
     d.keys_in = w + kin;
     d.keys_out = w + kout;
-    d.vals_in = vals ? reinterpret_cast<const uint32_t*>(w + vin) : nullptr;
-    d.vals_out = vals ? reinterpret_cast<uint32_t*>(w + vout) : nullptr;
+    d.vals_in = vals ? static_cast<const void*>(w + vin) : nullptr;
+    d.vals_out = vals ? static_cast<void*>(w + vout) : nullptr;
     d.n = n;
     d.begin_bit = begin_bit;
     d.end_bit = end_bit;
     d.temp = w;
-    d.temp_bytes = rs::temp_layout(key_bytes(key_type), vals, n, begin_bit, end_bit).total;
+    d.temp_bytes = rs::temp_layout(key_bytes(key_type), vals ? 4 : 0, n, begin_bit, end_bit).total;
     d.stream = stream;
     st = rs_sort(&d);
     if (st != RS_OK) return st;

@@ -54,24 +54,27 @@ constexpr int kRtsMaxCtas = 4096;
 #define RS_ITEMS_U32_KEYS 16
 #endif
 enum : int { kAlgoOnesweep = 1, kAlgoReduceScan = 2 };
-constexpr int tile_threads(int algo, int key_bytes, bool vals)
+// vb = bytes of the value that rides along each key: 0 (keys only), 4 or 8.
+constexpr int tile_threads(int algo, int key_bytes, int vb)
 {
     return algo == kAlgoOnesweep ? RS_OS_THREADS
            : key_bytes == 8      ? RS_RTS_THREADS_U64
-           : vals                ? RS_RTS_THREADS_PAIRS
+           : vb != 0             ? RS_RTS_THREADS_PAIRS
                                  : RS_RTS_THREADS;
 }
 #ifndef RS_ITEMS_U32_PAIRS
 #define RS_ITEMS_U32_PAIRS 12
 #endif
-constexpr int tile_items(int key_bytes, bool vals)
+constexpr int tile_items(int key_bytes, int vb)
 {
-    // 16-bit keys live in 32-bit registers: the 32-bit shapes
-    return key_bytes <= 4 ? (vals ? RS_ITEMS_U32_PAIRS : RS_ITEMS_U32_KEYS) : (vals ? 9 : 12);
+    // 16-bit keys live in 32-bit registers: the 32-bit shapes.  64-bit values
+    // take two registers each, so fewer keys per thread.
+    return key_bytes <= 4 ? (vb == 0 ? RS_ITEMS_U32_KEYS : vb == 4 ? RS_ITEMS_U32_PAIRS : 8)
+                          : (vb == 0 ? 12 : vb == 4 ? 9 : 6);
 }
-constexpr int tile_keys(int algo, int key_bytes, bool vals)
+constexpr int tile_keys(int algo, int key_bytes, int vb)
 {
-    return tile_threads(algo, key_bytes, vals) * tile_items(key_bytes, vals);
+    return tile_threads(algo, key_bytes, vb) * tile_items(key_bytes, vb);
 }
 
 // Small sorts: one kernel on a cluster of at most kClusterMaxCtas CTAs, each
@@ -91,21 +94,21 @@ constexpr int tile_keys(int algo, int key_bytes, bool vals)
 #endif
 constexpr int kClusterMaxCtas = RS_CL_MAX_CTAS;
 constexpr int kClusterThreads = RS_CL_THREADS;
-constexpr int cluster_items(int key_bytes, bool vals)
+constexpr int cluster_items(int key_bytes, int vb)
 {
-    // uint32 keys RS_CL_ITEMS per thread; 3/4 of that with values or for
-    // uint64 keys, 9/16 for uint64 keys with values (registers and shared
+    // uint32 keys RS_CL_ITEMS per thread; 3/4 of that with 32-bit values or
+    // for uint64 keys, less again with wider payloads (registers and shared
     // memory scale with the bytes per key)
-    return key_bytes <= 4 ? (vals ? RS_CL_ITEMS * 3 / 4 : RS_CL_ITEMS)
-                          : (vals ? RS_CL_ITEMS * 9 / 16 : RS_CL_ITEMS * 3 / 4);
+    return key_bytes <= 4 ? (vb == 0 ? RS_CL_ITEMS : vb == 4 ? RS_CL_ITEMS * 3 / 4 : RS_CL_ITEMS / 2)
+                          : (vb == 0 ? RS_CL_ITEMS * 3 / 4 : vb == 4 ? RS_CL_ITEMS * 9 / 16 : RS_CL_ITEMS * 3 / 8);
 }
-constexpr size_t cluster_tile_keys(int key_bytes, bool vals)
+constexpr size_t cluster_tile_keys(int key_bytes, int vb)
 {
-    return (size_t)kClusterThreads * cluster_items(key_bytes, vals);
+    return (size_t)kClusterThreads * cluster_items(key_bytes, vb);
 }
-constexpr size_t cluster_max_n(int key_bytes, bool vals)
+constexpr size_t cluster_max_n(int key_bytes, int vb)
 {
-    return (size_t)kClusterMaxCtas * cluster_tile_keys(key_bytes, vals);
+    return (size_t)kClusterMaxCtas * cluster_tile_keys(key_bytes, vb);
 }
 
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -120,21 +123,21 @@ constexpr int passes_for(int begin_bit, int end_bit, int radix_bits)
 struct TempLayout {
     size_t meta;       // kMetaWords uint32
     size_t alt_keys;   // n keys: the ping-pong partner of keys_out
-    size_t alt_vals;   // n values (pairs only)
+    size_t alt_vals;   // n values (pairs only; 4 or 8 bytes each)
     size_t big;        // chained-scan tile status, or reduce-then-scan block counts
     size_t big_bytes;
     size_t total;
 };
 
-constexpr size_t status_bytes(size_t n, int key_bytes, bool vals, int begin_bit, int end_bit,
+constexpr size_t status_bytes(size_t n, int key_bytes, int vb, int begin_bit, int end_bit,
                               int radix_bits)
 {
-    const size_t tk = (size_t)tile_keys(kAlgoOnesweep, key_bytes, vals);
+    const size_t tk = (size_t)tile_keys(kAlgoOnesweep, key_bytes, vb);
     size_t tiles = (n + tk - 1) / tk;
     return (size_t)passes_for(begin_bit, end_bit, radix_bits) * tiles * ((size_t)1 << radix_bits) * 4;
 }
 
-constexpr TempLayout temp_layout(int key_bytes, bool vals, size_t n, int begin_bit, int end_bit)
+constexpr TempLayout temp_layout(int key_bytes, int vb, size_t n, int begin_bit, int end_bit)
 {
     TempLayout t{};
     size_t off = 0;
@@ -143,10 +146,10 @@ constexpr TempLayout temp_layout(int key_bytes, bool vals, size_t n, int begin_b
     t.alt_keys = off;
     off += align_up(n * (size_t)key_bytes, 256);
     t.alt_vals = off;
-    off += vals ? align_up(n * 4, 256) : 0;
+    off += vb ? align_up(n * (size_t)vb, 256) : 0;
     t.big = off;
-    size_t s8 = status_bytes(n, key_bytes, vals, begin_bit, end_bit, 8);
-    size_t s4 = status_bytes(n, key_bytes, vals, begin_bit, end_bit, 4);
+    size_t s8 = status_bytes(n, key_bytes, vb, begin_bit, end_bit, 8);
+    size_t s4 = status_bytes(n, key_bytes, vb, begin_bit, end_bit, 4);
     size_t rts = (size_t)256 * kRtsMaxCtas * 4;
     size_t big = s8 > s4 ? s8 : s4;
     big = big > rts ? big : rts;

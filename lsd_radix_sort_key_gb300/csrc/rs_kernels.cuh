@@ -174,6 +174,11 @@ template <> struct KeyOps<KF16B> : KeyOps<KF16> { static constexpr bool kByte = 
 template <int KT, typename = void> struct IsByte { static constexpr bool value = false; };
 template <int KT> struct IsByte<KT, decltype((void)KeyOps<KT>::kByte)> { static constexpr bool value = true; };
 
+// The payload type by its byte count: 4 (uint32) or 8 (uint64); 0 = keys only.
+template <int VB> struct ValType { using type = uint32_t; };
+template <> struct ValType<8> { using type = uint64_t; };
+template <int VB> using ValT = typename ValType<VB>::type;
+
 // The digit of key u for a pass at `shift` of width mask; `flip` (mask for a
 // descending sort, else 0) reverses the digit order.  The byte twins serve
 // ascending sorts only.
@@ -277,14 +282,14 @@ struct PassParams {
     // actual ones from the sort-level buffers below (pass_buffers).
     const void* keys_in;
     void* keys_out;
-    const uint32_t* vals_in;
-    uint32_t* vals_out;
+    const void* vals_in;
+    void* vals_out;
     const void* sort_keys_in;   // the sort's input and output
     void* sort_keys_out;
-    const uint32_t* sort_vals_in;
-    uint32_t* sort_vals_out;
+    const void* sort_vals_in;
+    void* sort_vals_out;
     void* alt_keys;          // the ping-pong partner buffers in temp
-    uint32_t* alt_vals;
+    void* alt_vals;
     uint32_t* skip;          // the skip record in temp (see kSkipBase)
     uint32_t* plan;          // the pass plan in temp (see kPlanBase)
     uint32_t pass;           // this pass's index and the geometry of all passes
@@ -312,7 +317,7 @@ struct PassParams {
 };
 
 // Shared-memory layout of one tile (byte offsets, 16-byte aligned regions).
-template <typename T, int RB, int THREADS, int ITEMS, bool VALS>
+template <typename T, int RB, int THREADS, int ITEMS, int VB>
 struct TileSmem {
     static constexpr int BINS = 1 << RB;
     static constexpr int WARPS = THREADS / 32;
@@ -322,7 +327,7 @@ struct TileSmem {
     static constexpr int WH = BINS + 1;  // per-array counters + one dummy slot for tail lanes
     static constexpr size_t keys_off = 0;
     static constexpr size_t vals_off = align_up(sizeof(T) * TILE, 16);
-    static constexpr size_t wh_off = vals_off + (VALS ? align_up(4 * (size_t)TILE, 16) : 0);
+    static constexpr size_t wh_off = vals_off + (VB ? align_up(sizeof(ValT<VB>) * (size_t)TILE, 16) : 0);
     static constexpr size_t base_off = wh_off + align_up(4 * (size_t)VWARPS * WH, 16);
     static constexpr size_t scan_off = base_off + 4 * BINS;
     static constexpr size_t misc_off = scan_off + 4 * 32;
@@ -503,37 +508,37 @@ __host__ __device__ __forceinline__ bool chain_is_out(uint32_t i, uint32_t E, bo
 }
 
 // This pass's source and destination for role r.
-template <bool VALS>
+template <int VB>
 __device__ __forceinline__ void pass_buffers(PassParams& p, const PassRole& r)
 {
     const bool ip = p.in_place != 0u;
     const bool src_out = chain_is_out(r.j, r.E, ip), dst_out = chain_is_out(r.j + 1, r.E, ip);
     p.keys_in = r.j == 0 ? p.sort_keys_in : (src_out ? p.sort_keys_out : p.alt_keys);
     p.keys_out = dst_out ? p.sort_keys_out : p.alt_keys;
-    if constexpr (VALS) {
+    if constexpr (VB != 0) {
         p.vals_in = r.j == 0 ? p.sort_vals_in : (src_out ? p.sort_vals_out : p.alt_vals);
         p.vals_out = dst_out ? p.sort_vals_out : p.alt_vals;
     }
 }
 
 // Copy elements [lo, hi) of the keys (and values), thread t of `stride`.
-template <typename T, bool VALS>
-__device__ __forceinline__ void copy_span(const T* src, T* dst, const uint32_t* vsrc, uint32_t* vdst,
+template <typename T, int VB>
+__device__ __forceinline__ void copy_span(const T* src, T* dst, const void* vsrc, void* vdst,
                                           size_t lo, size_t hi, size_t t, size_t stride)
 {
     for (size_t i = lo + t; i < hi; i += stride) {
         dst[i] = src[i];
-        if constexpr (VALS) vdst[i] = vsrc[i];
+        if constexpr (VB != 0) static_cast<ValT<VB>*>(vdst)[i] = static_cast<const ValT<VB>*>(vsrc)[i];
     }
 }
 
 // When no pass runs, the last pass's kernel copies the input to the output
 // (out of place); its CTAs cover [lo, hi) each.
-template <typename T, bool VALS>
+template <typename T, int VB>
 __device__ __forceinline__ void copy_if_no_pass_runs(const PassParams& p, const PassRole& r, size_t lo, size_t hi)
 {
     if (r.E == 0u && p.pass + 1u == p.passes && p.in_place == 0u)
-        copy_span<T, VALS>(static_cast<const T*>(p.sort_keys_in), static_cast<T*>(p.sort_keys_out),
+        copy_span<T, VB>(static_cast<const T*>(p.sort_keys_in), static_cast<T*>(p.sort_keys_out),
                            p.sort_vals_in, p.sort_vals_out, lo, hi < p.n ? hi : p.n, threadIdx.x, blockDim.x);
 }
 
@@ -565,8 +570,8 @@ __device__ __forceinline__ void load_striped(const T* __restrict__ src, uint32_t
 struct PassIO {
     const void* keys_in;
     void* keys_out;
-    const uint32_t* vals_in;
-    uint32_t* vals_out;
+    const void* vals_in;
+    void* vals_out;
 };
 
 __device__ __forceinline__ void* lds_ptr(const void* slot)
@@ -600,39 +605,43 @@ __device__ __forceinline__ T* io_keys_out(const unsigned char* smem)
 {
     return static_cast<T*>(lds_ptr(&reinterpret_cast<const PassIO*>(smem + S::io_off)->keys_out));
 }
-template <typename S>
-__device__ __forceinline__ const uint32_t* io_vals_in(const unsigned char* smem)
+template <typename S, typename V>
+__device__ __forceinline__ const V* io_vals_in(const unsigned char* smem)
 {
-    return static_cast<const uint32_t*>(lds_ptr(&reinterpret_cast<const PassIO*>(smem + S::io_off)->vals_in));
+    return static_cast<const V*>(lds_ptr(&reinterpret_cast<const PassIO*>(smem + S::io_off)->vals_in));
 }
-template <typename S>
-__device__ __forceinline__ uint32_t* io_vals_out(const unsigned char* smem)
+template <typename S, typename V>
+__device__ __forceinline__ V* io_vals_out(const unsigned char* smem)
 {
-    return static_cast<uint32_t*>(lds_ptr(&reinterpret_cast<const PassIO*>(smem + S::io_off)->vals_out));
+    return static_cast<V*>(lds_ptr(&reinterpret_cast<const PassIO*>(smem + S::io_off)->vals_out));
 }
 
 // Keys (and values) of one tile in warp-striped order; a tile that runs past
 // n is guarded lane by lane.  The source is the pass's planned buffer
 // (p.keys_in), or with DYN the one in the PassIO slots.
-template <int KT, int RB, int THREADS, int ITEMS, bool VALS, bool DYN>
+template <int KT, int RB, int THREADS, int ITEMS, int VB, bool DYN>
 __device__ __forceinline__ void load_tile(const PassParams& p, const unsigned char* smem, uint32_t tile,
                                           typename KeyOps<KT>::T (&key)[ITEMS],
-                                          uint32_t (&val)[VALS ? ITEMS : 1])
+                                          ValT<VB> (&val)[VB ? ITEMS : 1])
 {
     using T = typename KeyOps<KT>::T;
-    using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
+    using S = TileSmem<T, RB, THREADS, ITEMS, VB>;
     constexpr uint32_t TILE = THREADS * ITEMS;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t seg = tile * TILE + (uint32_t)warp * (32u * ITEMS);
     const T* kin = DYN ? io_keys_in<S, T>(smem) : static_cast<const T*>(p.keys_in);
     if ((tile + 1) * TILE <= p.n) {
         load_striped<true, T, ITEMS>(kin, seg, p.n, lane, key);
-        if constexpr (VALS)
-            load_striped<true, uint32_t, ITEMS>(DYN ? io_vals_in<S>(smem) : p.vals_in, seg, p.n, lane, val);
+        if constexpr (VB != 0)
+            load_striped<true, ValT<VB>, ITEMS>(DYN ? io_vals_in<S, ValT<VB>>(smem)
+                                                    : static_cast<const ValT<VB>*>(p.vals_in),
+                                                seg, p.n, lane, val);
     } else {
         load_striped<false, T, ITEMS>(kin, seg, p.n, lane, key);
-        if constexpr (VALS)
-            load_striped<false, uint32_t, ITEMS>(DYN ? io_vals_in<S>(smem) : p.vals_in, seg, p.n, lane, val);
+        if constexpr (VB != 0)
+            load_striped<false, ValT<VB>, ITEMS>(DYN ? io_vals_in<S, ValT<VB>>(smem)
+                                                     : static_cast<const ValT<VB>*>(p.vals_in),
+                                                 seg, p.n, lane, val);
     }
 }
 
@@ -724,19 +733,19 @@ __device__ __forceinline__ void zero_counters(unsigned char* smem, int threads)
 // `publish(d, cnt)` runs for every digit as soon as the count is known (the
 // chained scan publishes it there).  The key/value registers are free again
 // on return (the caller prefetches the next tile into them).
-template <bool FULL, int KT, int RB, int THREADS, int ITEMS, bool VALS, typename Publish>
+template <bool FULL, int KT, int RB, int THREADS, int ITEMS, int VB, typename Publish>
 __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsigned char* smem,
                                                       uint32_t tile,
                                                       const typename KeyOps<KT>::T (&key)[ITEMS],
-                                                      const uint32_t (&val)[VALS ? ITEMS : 1],
+                                                      const ValT<VB> (&val)[VB ? ITEMS : 1],
                                                       uint32_t* cnt_out, uint32_t* start_out,
                                                       Publish publish)
 {
     using T = typename KeyOps<KT>::T;
-    using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
+    using S = TileSmem<T, RB, THREADS, ITEMS, VB>;
     constexpr int BINS = S::BINS, TILE = S::TILE, WH = S::WH, CHAINS = S::CHAINS, VWARPS = S::VWARPS;
     T* skeys = reinterpret_cast<T*>(smem + S::keys_off);
-    uint32_t* svals = reinterpret_cast<uint32_t*>(smem + S::vals_off);
+    ValT<VB>* svals = reinterpret_cast<ValT<VB>*>(smem + S::vals_off);
     uint32_t* whist = reinterpret_cast<uint32_t*>(smem + S::wh_off);
     uint32_t* sscan = reinterpret_cast<uint32_t*>(smem + S::scan_off);
 
@@ -786,7 +795,7 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
         pos = min(pos, (uint32_t)TILE - 1u);
         if (FULL || d < (uint32_t)BINS) {
             skeys[pos] = key[k];
-            if constexpr (VALS) svals[pos] = val[k];
+            if constexpr (VB != 0) svals[pos] = val[k];
         }
     }
     if (bad) record_error(p.err, RS_ERR_CHECK_FAILED);
@@ -799,15 +808,15 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
 // its tile-local start).  Consecutive slots mostly share a digit, so each
 // warp store covers few, contiguous segments.  Positions are bounds-checked
 // (a failure is recorded and the store skipped).
-template <bool FULL, int KT, int RB, int THREADS, int ITEMS, bool VALS>
+template <bool FULL, int KT, int RB, int THREADS, int ITEMS, int VB>
 __device__ __forceinline__ void tile_scatter(const PassParams& p, unsigned char* smem, uint32_t tile,
-                                             typename KeyOps<KT>::T* out, uint32_t* vout)
+                                             typename KeyOps<KT>::T* out, ValT<VB>* vout)
 {
     using T = typename KeyOps<KT>::T;
-    using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
+    using S = TileSmem<T, RB, THREADS, ITEMS, VB>;
     constexpr int TILE = S::TILE;
     const T* skeys = reinterpret_cast<const T*>(smem + S::keys_off);
-    const uint32_t* svals = reinterpret_cast<const uint32_t*>(smem + S::vals_off);
+    const ValT<VB>* svals = reinterpret_cast<const ValT<VB>*>(smem + S::vals_off);
     const uint32_t* sbase = reinterpret_cast<const uint32_t*>(smem + S::base_off);
     const uint32_t tile_base = tile * (uint32_t)TILE;
     const uint32_t valid = FULL ? (uint32_t)TILE : p.n - tile_base;
@@ -826,10 +835,10 @@ __device__ __forceinline__ void tile_scatter(const PassParams& p, unsigned char*
             if (ok) {
 #if RS_STORE_KEEP
                 st_keep(out + idx, kk, pol);
-                if constexpr (VALS) st_keep(vout + idx, svals[s], pol);
+                if constexpr (VB != 0) st_keep(vout + idx, svals[s], pol);
 #else
                 out[idx] = kk;
-                if constexpr (VALS) vout[idx] = svals[s];
+                if constexpr (VB != 0) vout[idx] = svals[s];
 #endif
             }
         }
@@ -911,13 +920,13 @@ __device__ __forceinline__ uint32_t lookback(const PassParams& p, uint32_t tile,
 // ------------------------------------------------------------------ kernels
 
 // One tile of a chained-scan pass.
-template <bool FULL, int KT, int RB, int THREADS, int ITEMS, bool VALS>
+template <bool FULL, int KT, int RB, int THREADS, int ITEMS, int VB>
 __device__ __forceinline__ void onesweep_tile(const PassParams& p, unsigned char* smem, uint32_t tile,
                                               const typename KeyOps<KT>::T (&key)[ITEMS],
-                                              const uint32_t (&val)[VALS ? ITEMS : 1])
+                                              const ValT<VB> (&val)[VB ? ITEMS : 1])
 {
     using T = typename KeyOps<KT>::T;
-    using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
+    using S = TileSmem<T, RB, THREADS, ITEMS, VB>;
     constexpr int BINS = S::BINS;
     uint32_t* sbase = reinterpret_cast<uint32_t*>(smem + S::base_off);
     uint32_t* sscan = reinterpret_cast<uint32_t*>(smem + S::scan_off);
@@ -932,7 +941,7 @@ __device__ __forceinline__ void onesweep_tile(const PassParams& p, unsigned char
 
     uint32_t cnt, start;
     uint32_t pre[RS_LOOKBACK_BATCH];
-    tile_rank_and_shuffle<FULL, KT, RB, THREADS, ITEMS, VALS>(
+    tile_rank_and_shuffle<FULL, KT, RB, THREADS, ITEMS, VB>(
         p, smem, tile, key, val, &cnt, &start, [&](int d, uint32_t c) {
             if (!stalled) {
                 if (tile == 0) st_relaxed_gpu(my_status + d, kFlagInc | ((gexcl + c) & kValMask));
@@ -949,18 +958,18 @@ __device__ __forceinline__ void onesweep_tile(const PassParams& p, unsigned char
         sbase[tid] = excl - start;
     }
     T* out = io_keys_out<S, T>(smem);
-    uint32_t* vout = VALS ? io_vals_out<S>(smem) : nullptr;
+    ValT<VB>* vout = VB ? io_vals_out<S, ValT<VB>>(smem) : nullptr;
     __syncthreads();
-    tile_scatter<FULL, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, out, vout);
+    tile_scatter<FULL, KT, RB, THREADS, ITEMS, VB>(p, smem, tile, out, vout);
 }
 
 // Chained-scan pass: one tile per CTA, in the order of an atomic ticket, so
 // every tile a CTA waits on belongs to a CTA that already runs.
-template <int KT, int RB, int THREADS, int ITEMS, bool VALS>
+template <int KT, int RB, int THREADS, int ITEMS, int VB>
 __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS) k_onesweep(PassParams p)
 {
     using T = typename KeyOps<KT>::T;
-    using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
+    using S = TileSmem<T, RB, THREADS, ITEMS, VB>;
     extern __shared__ __align__(16) unsigned char smem[];
     uint32_t* smisc = reinterpret_cast<uint32_t*>(smem + S::misc_off);
     const int tid = threadIdx.x;
@@ -974,7 +983,7 @@ __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS)
         publish_role(rsh, r);
         if (r.run) {
             PassParams q = p;
-            pass_buffers<VALS>(q, r);
+            pass_buffers<VB>(q, r);
             set_pass_io<S>(smem, q);
         }
     }
@@ -983,18 +992,18 @@ __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS)
     const PassRole role = read_role(rsh);
     if (!role.run) {
         const size_t lo = (size_t)blockIdx.x * S::TILE;
-        copy_if_no_pass_runs<T, VALS>(p, role, lo, lo + S::TILE);
+        copy_if_no_pass_runs<T, VB>(p, role, lo, lo + S::TILE);
         return;
     }
     const uint32_t tile = smisc[0];
     if (tile >= p.num_tiles) return;
     T key[ITEMS];
-    uint32_t val[VALS ? ITEMS : 1];
-    load_tile<KT, RB, THREADS, ITEMS, VALS, true>(p, smem, tile, key, val);
+    ValT<VB> val[VB ? ITEMS : 1];
+    load_tile<KT, RB, THREADS, ITEMS, VB, true>(p, smem, tile, key, val);
     if ((tile + 1) * (uint32_t)S::TILE <= p.n)
-        onesweep_tile<true, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, key, val);
+        onesweep_tile<true, KT, RB, THREADS, ITEMS, VB>(p, smem, tile, key, val);
     else
-        onesweep_tile<false, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, key, val);
+        onesweep_tile<false, KT, RB, THREADS, ITEMS, VB>(p, smem, tile, key, val);
 }
 
 // Reduce-then-scan, step 1: digit histogram of each CTA's chunk, written
@@ -1133,60 +1142,60 @@ __global__ void __launch_bounds__(THREADS) k_spine_scan(PassParams p, uint32_t* 
 
 // Reduce-then-scan, step 3: each CTA walks its chunk tile by tile, keeping a
 // running global offset per digit.
-template <bool FULL, int KT, int RB, int THREADS, int ITEMS, bool VALS, bool DYN>
+template <bool FULL, int KT, int RB, int THREADS, int ITEMS, int VB, bool DYN>
 __device__ __forceinline__ void downsweep_tile(const PassParams& p, unsigned char* smem, uint32_t tile,
                                                uint32_t next, uint32_t& running,
                                                typename KeyOps<KT>::T (&key)[ITEMS],
-                                               uint32_t (&val)[VALS ? ITEMS : 1])
+                                               ValT<VB> (&val)[VB ? ITEMS : 1])
 {
     using T = typename KeyOps<KT>::T;
-    using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
+    using S = TileSmem<T, RB, THREADS, ITEMS, VB>;
     constexpr int BINS = S::BINS;
     uint32_t* sbase = reinterpret_cast<uint32_t*>(smem + S::base_off);
     const int tid = threadIdx.x;
     uint32_t cnt, start;
-    tile_rank_and_shuffle<FULL, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, key, val, &cnt, &start,
+    tile_rank_and_shuffle<FULL, KT, RB, THREADS, ITEMS, VB>(p, smem, tile, key, val, &cnt, &start,
                                                                [](int, uint32_t) {});
-    if (next != 0xFFFFFFFFu) load_tile<KT, RB, THREADS, ITEMS, VALS, DYN>(p, smem, next, key, val);
+    if (next != 0xFFFFFFFFu) load_tile<KT, RB, THREADS, ITEMS, VB, DYN>(p, smem, next, key, val);
     T* out = DYN ? io_keys_out<S, T>(smem) : static_cast<T*>(p.keys_out);
-    uint32_t* vout = VALS ? (DYN ? io_vals_out<S>(smem) : p.vals_out) : nullptr;
+    ValT<VB>* vout = VB ? (DYN ? io_vals_out<S, ValT<VB>>(smem) : static_cast<ValT<VB>*>(p.vals_out)) : nullptr;
     if (tid < BINS) {
         sbase[tid] = running - start;
         running += cnt;
     }
     __syncthreads();
     zero_counters<S>(smem, THREADS);  // for the next tile; the scatter does not read them
-    tile_scatter<FULL, KT, RB, THREADS, ITEMS, VALS>(p, smem, tile, out, vout);
+    tile_scatter<FULL, KT, RB, THREADS, ITEMS, VB>(p, smem, tile, out, vout);
     __syncthreads();  // the next tile reuses shared memory
 }
 
 // The tile loop of one downsweep CTA.  DYN: the pass's buffers come from the
 // PassIO slots (some earlier pass was skipped) instead of the host's plan.
-template <int KT, int RB, int THREADS, int ITEMS, bool VALS, bool DYN>
+template <int KT, int RB, int THREADS, int ITEMS, int VB, bool DYN>
 __device__ __forceinline__ void downsweep_loop(const PassParams& p, unsigned char* smem, uint32_t running)
 {
     using T = typename KeyOps<KT>::T;
-    using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
+    using S = TileSmem<T, RB, THREADS, ITEMS, VB>;
     const uint32_t t0 = blockIdx.x * p.tiles_per_cta;
     const uint32_t t1 = min(p.num_tiles, t0 + p.tiles_per_cta);
     if (t0 >= t1) return;
     T key[ITEMS];
-    uint32_t val[VALS ? ITEMS : 1];
-    load_tile<KT, RB, THREADS, ITEMS, VALS, DYN>(p, smem, t0, key, val);
+    ValT<VB> val[VB ? ITEMS : 1];
+    load_tile<KT, RB, THREADS, ITEMS, VB, DYN>(p, smem, t0, key, val);
     for (uint32_t tile = t0; tile < t1; ++tile) {
         const uint32_t next = tile + 1 < t1 ? tile + 1 : 0xFFFFFFFFu;
         if ((tile + 1) * (uint32_t)S::TILE <= p.n)
-            downsweep_tile<true, KT, RB, THREADS, ITEMS, VALS, DYN>(p, smem, tile, next, running, key, val);
+            downsweep_tile<true, KT, RB, THREADS, ITEMS, VB, DYN>(p, smem, tile, next, running, key, val);
         else
-            downsweep_tile<false, KT, RB, THREADS, ITEMS, VALS, DYN>(p, smem, tile, next, running, key, val);
+            downsweep_tile<false, KT, RB, THREADS, ITEMS, VB, DYN>(p, smem, tile, next, running, key, val);
     }
 }
 
-template <int KT, int RB, int THREADS, int ITEMS, bool VALS>
+template <int KT, int RB, int THREADS, int ITEMS, int VB>
 __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS) k_downsweep(PassParams p)
 {
     using T = typename KeyOps<KT>::T;
-    using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
+    using S = TileSmem<T, RB, THREADS, ITEMS, VB>;
     constexpr int BINS = S::BINS;
     extern __shared__ __align__(16) unsigned char smem[];
     uint32_t* sscan = reinterpret_cast<uint32_t*>(smem + S::scan_off);
@@ -1202,7 +1211,7 @@ __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS)
         publish_role(rsh, r);
         if (r.run && r.E != p.passes) {
             PassParams q = p;
-            pass_buffers<VALS>(q, r);
+            pass_buffers<VB>(q, r);
             set_pass_io<S>(smem, q);
         }
     }
@@ -1212,25 +1221,25 @@ __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS)
     const PassRole role = read_role(rsh);
     if (!role.run) {
         const size_t lo = (size_t)g * p.tiles_per_cta * S::TILE;
-        copy_if_no_pass_runs<T, VALS>(p, role, lo, lo + (size_t)p.tiles_per_cta * S::TILE);
+        copy_if_no_pass_runs<T, VB>(p, role, lo, lo + (size_t)p.tiles_per_cta * S::TILE);
         return;
     }
     const uint32_t running = tid < BINS ? dstart + block_off : 0u;
     if (role.E == p.passes)  // every pass runs: the host's plan holds
-        downsweep_loop<KT, RB, THREADS, ITEMS, VALS, false>(p, smem, running);
+        downsweep_loop<KT, RB, THREADS, ITEMS, VB, false>(p, smem, running);
     else
-        downsweep_loop<KT, RB, THREADS, ITEMS, VALS, true>(p, smem, running);
+        downsweep_loop<KT, RB, THREADS, ITEMS, VB, true>(p, smem, running);
 }
 
 // In place with an odd number of running passes the result ends in the
 // partner buffer (see chain_is_out): copy it back to keys_out.
-template <int RB, typename T, bool VALS>
+template <int RB, typename T, int VB>
 __global__ void __launch_bounds__(256) k_chain_copy(PassParams p)
 {
     __shared__ RoleShared rsh;
     const PassRole role = block_pass_role(p, &rsh);
     if (p.in_place == 0u || role.E % 2u == 0u) return;
-    copy_span<T, VALS>(static_cast<const T*>(p.alt_keys), static_cast<T*>(p.sort_keys_out), p.alt_vals,
+    copy_span<T, VB>(static_cast<const T*>(p.alt_keys), static_cast<T*>(p.sort_keys_out), p.alt_vals,
                        p.sort_vals_out, 0, p.n, (size_t)blockIdx.x * blockDim.x + threadIdx.x,
                        (size_t)gridDim.x * blockDim.x);
 }
@@ -1252,8 +1261,8 @@ __global__ void __launch_bounds__(256) k_chain_copy(PassParams p)
 struct ClusterParams {
     const void* keys_in;
     void* keys_out;
-    const uint32_t* vals_in;
-    uint32_t* vals_out;
+    const void* vals_in;
+    void* vals_out;
     uint32_t n;
     uint32_t passes;
     uint32_t begin_bit;
@@ -1263,33 +1272,33 @@ struct ClusterParams {
     uint32_t descending;
 };
 
-template <typename T, int RB, int THREADS, int ITEMS, bool VALS>
+template <typename T, int RB, int THREADS, int ITEMS, int VB>
 struct ClusterSmem {
-    using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
+    using S = TileSmem<T, RB, THREADS, ITEMS, VB>;
     static constexpr size_t next_keys_off = align_up(S::bytes, 16);  // this CTA's keys of the next pass
     static constexpr size_t next_vals_off = next_keys_off + align_up(sizeof(T) * S::TILE, 16);
-    static constexpr size_t cnt_off = next_vals_off + (VALS ? align_up(4 * (size_t)S::TILE, 16) : 0);
+    static constexpr size_t cnt_off = next_vals_off + (VB ? align_up(sizeof(ValT<VB>) * (size_t)S::TILE, 16) : 0);
     static constexpr size_t rec_off = cnt_off + 4 * S::BINS;  // this CTA's share of the skip record
     static constexpr size_t plan_off = rec_off + 16;          // run mask, running passes
     static constexpr size_t bytes = plan_off + 16;
 };
 
-template <int KT, int RB, int THREADS, int ITEMS, bool VALS>
+template <int KT, int RB, int THREADS, int ITEMS, int VB>
 __global__ void __launch_bounds__(THREADS, 1) k_cluster_sort(ClusterParams cp)
 {
     namespace cg = cooperative_groups;
     using T = typename KeyOps<KT>::T;
-    using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
-    using CS = ClusterSmem<T, RB, THREADS, ITEMS, VALS>;
+    using S = TileSmem<T, RB, THREADS, ITEMS, VB>;
+    using CS = ClusterSmem<T, RB, THREADS, ITEMS, VB>;
     constexpr int BINS = S::BINS;
     constexpr uint32_t M = S::TILE;
     extern __shared__ __align__(16) unsigned char smem[];
     const T* skeys = reinterpret_cast<const T*>(smem + S::keys_off);
-    const uint32_t* svals = reinterpret_cast<const uint32_t*>(smem + S::vals_off);
+    const ValT<VB>* svals = reinterpret_cast<const ValT<VB>*>(smem + S::vals_off);
     uint32_t* sbase = reinterpret_cast<uint32_t*>(smem + S::base_off);
     uint32_t* sscan = reinterpret_cast<uint32_t*>(smem + S::scan_off);
     T* nkeys = reinterpret_cast<T*>(smem + CS::next_keys_off);
-    uint32_t* nvals = reinterpret_cast<uint32_t*>(smem + CS::next_vals_off);
+    ValT<VB>* nvals = reinterpret_cast<ValT<VB>*>(smem + CS::next_vals_off);
     uint32_t* cnts = reinterpret_cast<uint32_t*>(smem + CS::cnt_off);
     uint32_t* rec = reinterpret_cast<uint32_t*>(smem + CS::rec_off);
     uint32_t* plan = reinterpret_cast<uint32_t*>(smem + CS::plan_off);
@@ -1307,13 +1316,15 @@ __global__ void __launch_bounds__(THREADS, 1) k_cluster_sort(ClusterParams cp)
 
     // 1. This CTA's keys, warp-striped (as load_tile), from global memory.
     T key[ITEMS];
-    uint32_t val[VALS ? ITEMS : 1];
+    ValT<VB> val[VB ? ITEMS : 1];
     if (valid == M) {
         load_striped<true, T, ITEMS>(gin + lo, seg, valid, lane, key);
-        if constexpr (VALS) load_striped<true, uint32_t, ITEMS>(cp.vals_in + lo, seg, valid, lane, val);
+        if constexpr (VB != 0)
+            load_striped<true, ValT<VB>, ITEMS>(static_cast<const ValT<VB>*>(cp.vals_in) + lo, seg, valid, lane, val);
     } else {
         load_striped<false, T, ITEMS>(gin + lo, seg, valid, lane, key);
-        if constexpr (VALS) load_striped<false, uint32_t, ITEMS>(cp.vals_in + lo, seg, valid, lane, val);
+        if constexpr (VB != 0)
+            load_striped<false, ValT<VB>, ITEMS>(static_cast<const ValT<VB>*>(cp.vals_in) + lo, seg, valid, lane, val);
     }
 
     // 2. The skip record: each CTA's share of diff and of the order check
@@ -1380,10 +1391,10 @@ __global__ void __launch_bounds__(THREADS, 1) k_cluster_sort(ClusterParams cp)
         if (j > 0) {  // this CTA's keys of this pass, left by the previous one
             if (valid == M) {
                 load_striped<true, T, ITEMS>(nkeys, seg, valid, lane, key);
-                if constexpr (VALS) load_striped<true, uint32_t, ITEMS>(nvals, seg, valid, lane, val);
+                if constexpr (VB != 0) load_striped<true, ValT<VB>, ITEMS>(nvals, seg, valid, lane, val);
             } else {
                 load_striped<false, T, ITEMS>(nkeys, seg, valid, lane, key);
-                if constexpr (VALS) load_striped<false, uint32_t, ITEMS>(nvals, seg, valid, lane, val);
+                if constexpr (VB != 0) load_striped<false, ValT<VB>, ITEMS>(nvals, seg, valid, lane, val);
             }
         }
         p.shift = cp.begin_bit + q * RB;
@@ -1393,10 +1404,10 @@ __global__ void __launch_bounds__(THREADS, 1) k_cluster_sort(ClusterParams cp)
         __syncthreads();
         uint32_t cnt, start;
         if (valid == M)
-            tile_rank_and_shuffle<true, KT, RB, THREADS, ITEMS, VALS>(p, smem, 0, key, val, &cnt, &start,
+            tile_rank_and_shuffle<true, KT, RB, THREADS, ITEMS, VB>(p, smem, 0, key, val, &cnt, &start,
                                                                       [](int, uint32_t) {});
         else
-            tile_rank_and_shuffle<false, KT, RB, THREADS, ITEMS, VALS>(p, smem, 0, key, val, &cnt, &start,
+            tile_rank_and_shuffle<false, KT, RB, THREADS, ITEMS, VB>(p, smem, 0, key, val, &cnt, &start,
                                                                        [](int, uint32_t) {});
         if (tid < BINS) cnts[tid] = cnt;
         // Counts published; every CTA has also read its keys of this pass, so
@@ -1428,11 +1439,11 @@ __global__ void __launch_bounds__(THREADS, 1) k_cluster_sort(ClusterParams cp)
                 }
                 if (last) {
                     gout[g] = kk;
-                    if constexpr (VALS) cp.vals_out[g] = svals[s];
+                    if constexpr (VB != 0) static_cast<ValT<VB>*>(cp.vals_out)[g] = svals[s];
                 } else {
                     const uint32_t dst = g / M, off = g - dst * M;
                     *cluster.map_shared_rank(nkeys + off, dst) = kk;
-                    if constexpr (VALS) *cluster.map_shared_rank(nvals + off, dst) = svals[s];
+                    if constexpr (VB != 0) *cluster.map_shared_rank(nvals + off, dst) = svals[s];
                 }
             }
         }
@@ -1442,7 +1453,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_cluster_sort(ClusterParams cp)
     }
     // No pass runs: the input is the result.
     if (E == 0u && cp.keys_in != cp.keys_out)
-        copy_span<T, VALS>(gin, static_cast<T*>(cp.keys_out), cp.vals_in, cp.vals_out, lo, lo + valid, tid,
+        copy_span<T, VB>(gin, static_cast<T*>(cp.keys_out), cp.vals_in, cp.vals_out, lo, lo + valid, tid,
                            THREADS);
 }
 
@@ -1579,6 +1590,7 @@ __global__ void __launch_bounds__(THREADS) k_histogram(HistParams h)
 struct Plan {
     int kt;
     bool vals;
+    int vb;           // value bytes: 0, 4 or 8
     size_t n;
     int begin_bit, end_bit;
     int algo;         // RS_ALGO_ONESWEEP or RS_ALGO_REDUCE_SCAN (resolved)
@@ -1587,8 +1599,8 @@ struct Plan {
     int passes;
     const void* keys_in;
     void* keys_out;
-    const uint32_t* vals_in;
-    uint32_t* vals_out;
+    const void* vals_in;
+    void* vals_out;
     unsigned char* temp;
     TempLayout lay;
     cudaStream_t stream;
@@ -1651,18 +1663,18 @@ template <> struct ByteTwin<KU16> { static constexpr int value = KU16B; };
 template <> struct ByteTwin<KI16> { static constexpr int value = KI16B; };
 template <> struct ByteTwin<KF16> { static constexpr int value = KF16B; };
 
-template <int KT, int RB, bool VALS>
+template <int KT, int RB, int VB>
 rs_status run_passes(Plan& pl)
 {
     using T = typename KeyOps<KT>::T;
     constexpr int KB = sizeof(T);
-    constexpr int ITEMS = tile_items(KB, VALS);
+    constexpr int ITEMS = tile_items(KB, VB);
     constexpr int BINS = 1 << RB;
     const uint32_t n = (uint32_t)pl.n;
     uint32_t* meta = reinterpret_cast<uint32_t*>(pl.temp + pl.lay.meta);
     uint32_t* big = reinterpret_cast<uint32_t*>(pl.temp + pl.lay.big);
     T* alt_keys = reinterpret_cast<T*>(pl.temp + pl.lay.alt_keys);
-    uint32_t* alt_vals = reinterpret_cast<uint32_t*>(pl.temp + pl.lay.alt_vals);
+    void* alt_vals = pl.temp + pl.lay.alt_vals;
     const int P = pl.passes;
 
     // The host plans each pass's buffers for the case where every pass runs
@@ -1672,10 +1684,10 @@ rs_status run_passes(Plan& pl)
     PassParams base{};
     base.sort_keys_in = pl.keys_in;
     base.sort_keys_out = pl.keys_out;
-    base.sort_vals_in = VALS ? pl.vals_in : nullptr;
-    base.sort_vals_out = VALS ? pl.vals_out : nullptr;
+    base.sort_vals_in = (VB != 0) ? pl.vals_in : nullptr;
+    base.sort_vals_out = (VB != 0) ? pl.vals_out : nullptr;
     base.alt_keys = alt_keys;
-    base.alt_vals = VALS ? alt_vals : nullptr;
+    base.alt_vals = (VB != 0) ? alt_vals : nullptr;
     base.skip = meta + kSkipBase;
     base.plan = meta + kPlanBase;
     base.passes = (uint32_t)P;
@@ -1694,8 +1706,8 @@ rs_status run_passes(Plan& pl)
         const bool src_out = chain_is_out(j, E, in_place), dst_out = chain_is_out(j + 1, E, in_place);
         pp.keys_in = j == 0 ? pl.keys_in : (src_out ? pl.keys_out : static_cast<const void*>(alt_keys));
         pp.keys_out = dst_out ? pl.keys_out : static_cast<void*>(alt_keys);
-        if (VALS) {
-            pp.vals_in = j == 0 ? pl.vals_in : (src_out ? pl.vals_out : alt_vals);
+        if (VB != 0) {
+            pp.vals_in = j == 0 ? pl.vals_in : (src_out ? static_cast<const void*>(pl.vals_out) : alt_vals);
             pp.vals_out = dst_out ? pl.vals_out : alt_vals;
         }
     };
@@ -1703,22 +1715,22 @@ rs_status run_passes(Plan& pl)
     // In place, a final copy (k_chain_copy) runs when an odd number of passes ran.
     auto finish = [&]() -> rs_status {
         if (!in_place) return RS_OK;
-        if (!pl.count_only) k_chain_copy<RB, T, VALS><<<4 * sms, 256, 0, pl.stream>>>(base);
+        if (!pl.count_only) k_chain_copy<RB, T, VB><<<4 * sms, 256, 0, pl.stream>>>(base);
         return after_launch(pl, kKindCopy);
     };
 
     if (pl.algo == RS_ALGO_ONESWEEP) {
-        constexpr int THREADS = tile_threads(kAlgoOnesweep, KB, VALS);
+        constexpr int THREADS = tile_threads(kAlgoOnesweep, KB, VB);
         constexpr int TILE = THREADS * ITEMS;
-        using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
+        using S = TileSmem<T, RB, THREADS, ITEMS, VB>;
         const uint32_t num_tiles = (n + TILE - 1) / TILE;
         base.num_tiles = num_tiles;
         constexpr int MAXP = (8 * KB + RB - 1) / RB;
         constexpr int HCOLS = (MAXP * (1 << RB) * 32 * 4 <= 160 * 1024) ? 32 : 16;
         const bool full_range = pl.begin_bit == 0 && pl.end_bit == 8 * KB;
         auto hk = full_range ? k_histogram<KT, RB, 1024, HCOLS, true> : k_histogram<KT, RB, 1024, HCOLS, false>;
-        auto pk = k_onesweep<KT, RB, THREADS, ITEMS, VALS>;
-        auto pkb = k_onesweep<ByteTwin<KT>::value, RB, THREADS, ITEMS, VALS>;
+        auto pk = k_onesweep<KT, RB, THREADS, ITEMS, VB>;
+        auto pkb = k_onesweep<ByteTwin<KT>::value, RB, THREADS, ITEMS, VB>;
         if (!pl.count_only && (!set_smem(pk, S::bytes) || !set_smem(pkb, S::bytes))) return RS_ERR_CUDA;
         const size_t status_words = (size_t)P * num_tiles * BINS;
         HistParams h{};
@@ -1762,16 +1774,16 @@ rs_status run_passes(Plan& pl)
     }
 
     // Reduce-then-scan.
-    constexpr int THREADS = tile_threads(kAlgoReduceScan, KB, VALS);
+    constexpr int THREADS = tile_threads(kAlgoReduceScan, KB, VB);
     constexpr int TILE = THREADS * ITEMS;
-    using S = TileSmem<T, RB, THREADS, ITEMS, VALS>;
+    using S = TileSmem<T, RB, THREADS, ITEMS, VB>;
     const uint32_t num_tiles = (n + TILE - 1) / TILE;
     base.num_tiles = num_tiles;
     const bool full_range = pl.begin_bit == 0 && pl.end_bit == 8 * KB;
     auto uk0 = full_range ? k_upsweep<KT, RB, 512, TILE, true, true> : k_upsweep<KT, RB, 512, TILE, true, false>;
     auto uk = k_upsweep<KT, RB, 512, TILE, false>;
-    auto dk = k_downsweep<KT, RB, THREADS, ITEMS, VALS>;
-    auto dkb = k_downsweep<ByteTwin<KT>::value, RB, THREADS, ITEMS, VALS>;
+    auto dk = k_downsweep<KT, RB, THREADS, ITEMS, VB>;
+    auto dkb = k_downsweep<ByteTwin<KT>::value, RB, THREADS, ITEMS, VB>;
     if (!pl.count_only && (!set_smem(dk, S::bytes) || !set_smem(dkb, S::bytes))) return RS_ERR_CUDA;
     uint32_t G = 1;
     if (!pl.count_only) {
@@ -1843,35 +1855,35 @@ inline unsigned max_cluster_ctas(K kernel, int threads, size_t smem_bytes)
 }
 
 // CTAs the cluster sort of n keys needs, or 0 if this device cannot run it.
-template <int KT, int RB, bool VALS>
+template <int KT, int RB, int VB>
 unsigned cluster_ctas_for(size_t n)
 {
     using T = typename KeyOps<KT>::T;
     constexpr int KB = sizeof(T);
-    constexpr int ITEMS = cluster_items(KB, VALS);
-    using CS = ClusterSmem<T, RB, kClusterThreads, ITEMS, VALS>;
-    const size_t tile = cluster_tile_keys(KB, VALS);
+    constexpr int ITEMS = cluster_items(KB, VB);
+    using CS = ClusterSmem<T, RB, kClusterThreads, ITEMS, VB>;
+    const size_t tile = cluster_tile_keys(KB, VB);
     const size_t ctas = (n + tile - 1) / tile;
     if (ctas < 1 || ctas > (size_t)kClusterMaxCtas) return 0;
     if (ctas <= 8) return (unsigned)ctas;  // the portable size always schedules
-    const unsigned cap = max_cluster_ctas(k_cluster_sort<KT, RB, kClusterThreads, ITEMS, VALS>,
+    const unsigned cap = max_cluster_ctas(k_cluster_sort<KT, RB, kClusterThreads, ITEMS, VB>,
                                           kClusterThreads, CS::bytes);
     return ctas <= cap ? (unsigned)ctas : 0u;
 }
 
 // The whole sort as one launch on a cluster of ceil(n / tile) CTAs.
-template <int KT, int RB, bool VALS>
+template <int KT, int RB, int VB>
 rs_status run_cluster(Plan& pl)
 {
     using T = typename KeyOps<KT>::T;
     constexpr int KB = sizeof(T);
-    constexpr int ITEMS = cluster_items(KB, VALS);
+    constexpr int ITEMS = cluster_items(KB, VB);
     constexpr int THREADS = kClusterThreads;
-    using CS = ClusterSmem<T, RB, THREADS, ITEMS, VALS>;
-    const unsigned ctas = cluster_ctas_for<KT, RB, VALS>(pl.n);
+    using CS = ClusterSmem<T, RB, THREADS, ITEMS, VB>;
+    const unsigned ctas = cluster_ctas_for<KT, RB, VB>(pl.n);
     if (ctas == 0) return RS_ERR_UNSUPPORTED;
     if (pl.count_only) return after_launch(pl, kKindCluster);
-    auto kernel = k_cluster_sort<KT, RB, THREADS, ITEMS, VALS>;
+    auto kernel = k_cluster_sort<KT, RB, THREADS, ITEMS, VB>;
     if (!set_smem(kernel, CS::bytes)) return RS_ERR_CUDA;
     if (ctas > 8 && cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
         return RS_ERR_CUDA;
@@ -1879,8 +1891,8 @@ rs_status run_cluster(Plan& pl)
     ClusterParams cp{};
     cp.keys_in = pl.keys_in;
     cp.keys_out = pl.keys_out;
-    cp.vals_in = VALS ? pl.vals_in : nullptr;
-    cp.vals_out = VALS ? pl.vals_out : nullptr;
+    cp.vals_in = (VB != 0) ? pl.vals_in : nullptr;
+    cp.vals_out = (VB != 0) ? pl.vals_out : nullptr;
     cp.n = (uint32_t)pl.n;
     cp.passes = (uint32_t)pl.passes;
     cp.begin_bit = (uint32_t)pl.begin_bit;
@@ -1904,27 +1916,30 @@ rs_status run_cluster(Plan& pl)
     return after_launch(pl, kKindCluster);
 }
 
-template <int KT>
-rs_status run_sort(Plan& pl)
+// The instantiation for this request's digit width and value bytes.
+template <int KT, int VB>
+rs_status run_sort_vb(Plan& pl)
 {
     if (pl.algo == RS_ALGO_CLUSTER) {
-        const unsigned ctas = pl.vals ? (pl.radix_bits == 4 ? cluster_ctas_for<KT, 4, true>(pl.n)
-                                                            : cluster_ctas_for<KT, 8, true>(pl.n))
-                                      : (pl.radix_bits == 4 ? cluster_ctas_for<KT, 4, false>(pl.n)
-                                                            : cluster_ctas_for<KT, 8, false>(pl.n));
+        const unsigned ctas = pl.radix_bits == 4 ? cluster_ctas_for<KT, 4, VB>(pl.n)
+                                                 : cluster_ctas_for<KT, 8, VB>(pl.n);
         if (ctas == 0 && pl.auto_chosen) {
             pl.algo = RS_ALGO_ONESWEEP;  // this device cannot schedule the cluster
         } else {
-            if (pl.vals) return pl.radix_bits == 4 ? run_cluster<KT, 4, true>(pl) : run_cluster<KT, 8, true>(pl);
-            return pl.radix_bits == 4 ? run_cluster<KT, 4, false>(pl) : run_cluster<KT, 8, false>(pl);
+            return pl.radix_bits == 4 ? run_cluster<KT, 4, VB>(pl) : run_cluster<KT, 8, VB>(pl);
         }
     }
-    if (pl.vals) {
-        if (pl.radix_bits == 4) return run_passes<KT, 4, true>(pl);
-        return run_passes<KT, 8, true>(pl);
+    return pl.radix_bits == 4 ? run_passes<KT, 4, VB>(pl) : run_passes<KT, 8, VB>(pl);
+}
+
+template <int KT>
+rs_status run_sort(Plan& pl)
+{
+    switch (pl.vb) {
+    case 0: return run_sort_vb<KT, 0>(pl);
+    case 8: return run_sort_vb<KT, 8>(pl);
+    default: return run_sort_vb<KT, 4>(pl);
     }
-    if (pl.radix_bits == 4) return run_passes<KT, 4, false>(pl);
-    return run_passes<KT, 8, false>(pl);
 }
 
 }  // namespace rs

@@ -25,7 +25,7 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = rs::temp_layout(4, false, RS_NOALLOC_MAX_N, 0, 32).total;
+constexpr size_t kScratchBytes = rs::temp_layout(4, 0, RS_NOALLOC_MAX_N, 0, 32).total;
 static_assert(kScratchBytes <= RS_NOALLOC_SCRATCH_BYTES, "scratch size in rs.h is too small");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[RS_NOALLOC_SCRATCH_BYTES];

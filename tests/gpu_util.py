@@ -32,25 +32,27 @@ def gpu_sort(kt, keys, vals=None, begin_bit=0, end_bit=None, algo="auto", radix_
     kin = kin_full[offset:]
     vin = None
     if vals is not None:
-        vin_full = to_dev(np.concatenate([np.zeros(offset, np.uint32), vals]) if offset else vals, dev)
+        vin_full = to_dev(np.concatenate([np.zeros(offset, vals.dtype), vals]) if offset else vals, dev)
         vin = vin_full[offset:]
     if in_place:
         kout, vout = kin, vin
     else:
         kout = torch.empty_like(kin) if n else kin
         vout = None if vin is None else (torch.empty_like(vin) if n else vin)
-    tb = rs.rs_temp_bytes(kt, vals is not None, n, begin_bit, end_bit)
+    vb = 0 if vals is None else vals.dtype.itemsize
+    tb = rs.rs_temp_bytes(kt, vb if vb else False, n, begin_bit, end_bit)
     temp = torch.empty(max(tb, 256), dtype=torch.uint8, device=dev)
     d = rs.make_desc(kt, kin if n else None, kout if n else None, vin if n else None,
                      vout if n else None, n, begin_bit, end_bit, temp, temp.numel(),
-                     None, algo, radix_bits, descending=descending)
+                     None, algo, radix_bits, descending=descending, value_bytes=vb)
     st = rs.rs_sort(d)
     assert st == 0, rs.STATUS.get(st, st)
     torch.cuda.synchronize()
     if check_status and n:
         assert rs.rs_device_status(temp) == 0
     ko = kout.cpu().numpy().view(NP_KEY[kt]) if n else np.empty(0, NP_KEY[kt])
-    vo = None if vals is None else (vout.cpu().numpy().view(np.uint32) if n else np.empty(0, np.uint32))
+    vdt = np.uint64 if vb == 8 else np.uint32
+    vo = None if vals is None else (vout.cpu().numpy().view(vdt) if n else np.empty(0, vdt))
     assert kb == ko.dtype.itemsize
     if want_record:
         st, bits, unordered = rs.rs_skip_record(temp)

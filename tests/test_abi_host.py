@@ -143,6 +143,27 @@ def test_cluster_capacity(lib):
     assert rs.rs_cluster_max_n("u64", True) == 16 * 512 * 4
 
 
+def test_64bit_values_shape_and_checks(lib):
+    n = 1 << 20
+    assert rs.rs_temp_bytes("u32", 8, n, 0, 32) >= rs.rs_temp_bytes("u32", True, n, 0, 32) + 4 * n
+    assert rs.rs_cluster_max_n("u32", 8) == 16 * 512 * 4
+    assert rs.rs_cluster_max_n("u64", 8) == 16 * 512 * 3
+    tb = rs.rs_temp_bytes("u32", 8, 1000, 0, 32)
+
+    def d(**kw):
+        base = dict(vals_in=4 * FAKE, vals_out=5 * FAKE, value_bytes=8)
+        base.update(kw)
+        return rs.make_desc("u32", FAKE, 2 * FAKE, base["vals_in"], base["vals_out"], 1000, 0, 32,
+                            3 * FAKE, tb, 0, "onesweep", 0, value_bytes=base["value_bytes"])
+    assert rs.rs_sort_kernel_count(d()) == 1 + 4
+    assert rs.rs_sort(d(value_bytes=3)) == 1                     # not 0, 4 or 8
+    assert rs.rs_sort(d(vals_in=4 * FAKE + 4)) == 1              # 4-byte aligned, needs 8
+    # the same buffer holds 1000 uint64 values only if temp was sized for them
+    assert rs.rs_sort(rs.make_desc("u32", FAKE, 2 * FAKE, 4 * FAKE, 5 * FAKE, 1000, 0, 32, 3 * FAKE,
+                                   rs.rs_temp_bytes("u32", True, 1000, 0, 32), 0, "onesweep", 0,
+                                   value_bytes=8)) == 2
+
+
 def test_status_strings(lib):
     for code in range(8):
         assert rs.rs_status_string(code)

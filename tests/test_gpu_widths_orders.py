@@ -1,11 +1,13 @@
-"""16-bit keys and descending order, bit-exact against the CPU oracle (needs a GPU).
+"""16-bit keys, descending order and 64-bit payloads, bit-exact against the
+CPU oracle (needs a GPU).
 
 uint16, int16 and binary16 keys under every schedule and both digit widths,
 with and without values, full and partial bit ranges, in place, unaligned
 and through the typed entry points; descending order for every key type,
 including the inputs that skip passes (already in ascending order: nothing
 skipped; already in descending order: every pass skipped), whose skip record
-is checked against its definition.
+is checked against its definition; uint64 payloads for 32-, 64- and 16-bit
+keys (expected payloads gathered by the oracle's permutation).
 """
 import numpy as np
 import pytest
@@ -123,3 +125,48 @@ def test_descending_partial_ranges_ties_and_skips(algo):
         got, _, rec = gpu_sort("u32", inp, None, 0, 32, algo=algo, descending=True, want_record=True)
         assert np.array_equal(got, down)
         assert rec[1] == unordered
+
+
+def check64(kt, keys, b, e, descending=False, **kw):
+    """64-bit payloads: the oracle gives the permutation (values = index) and
+    the expected payloads are the random 64-bit values gathered by it."""
+    n = len(keys)
+    vals64 = synth.u64_uniform(n, 4242 + n)
+    got_k, got_v = gpu_sort(kt, keys, vals64, b, e, descending=descending, **kw)
+    ref_k, perm = oracle.sort(kt, keys, synth.iota_u32(n), b, e, descending=descending)
+    assert np.array_equal(got_k, ref_k), f"keys differ ({kt}, n={n}, {kw})"
+    assert got_v.dtype == np.uint64 and np.array_equal(got_v, vals64[perm]), f"values differ ({kt}, n={n}, {kw})"
+
+
+def sizes64(algo, kt):
+    if algo == "cluster":
+        cap = rs.rs_cluster_max_n(kt, 8)
+        return [1, 31, cap // 3, cap]
+    return [1, 3841, 300_001]
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("kt", ["u32", "f32", "u64", "u16"])
+def test_64bit_values(algo, kt):
+    for i, n in enumerate(sizes64(algo, kt)):
+        check64(kt, gen_keys(kt, n, 1200 + i), 0, rs.KEY_BITS[kt], algo=algo)
+    n = sizes64(algo, kt)[-1]
+    keys = gen_keys(kt, n, 1210)
+    check64(kt, keys, 0, rs.KEY_BITS[kt], algo=algo, radix_bits=4)
+    check64(kt, keys, 0, rs.KEY_BITS[kt], algo=algo, descending=True)
+    check64(kt, keys, 0, rs.KEY_BITS[kt], algo=algo, in_place=True)
+    if kt in ("u32", "u64", "u16"):
+        check64(kt, keys, 3, rs.KEY_BITS[kt] - 2, algo=algo)
+
+
+def test_64bit_values_unaligned_keys_and_sort_wrapper():
+    n = 100_003
+    keys = synth.u32_uniform(n, 1220)
+    check64("u32", keys, 0, 32, offset=1)   # keys 4-byte aligned only; values still 8-byte aligned
+    kin = to_dev(keys, "cuda:0")
+    vin = to_dev(synth.u64_uniform(n, 1221), "cuda:0")
+    ko, vo = rs.sort(kin, vin, key_type="u32", descending=True)
+    torch.cuda.synchronize()
+    ref_k, perm = oracle.sort("u32", keys, synth.iota_u32(n), 0, 32, descending=True)
+    assert np.array_equal(ko.cpu().numpy().view(np.uint32), ref_k)
+    assert np.array_equal(vo.cpu().numpy().view(np.uint64), synth.u64_uniform(n, 1221)[perm])
