@@ -66,37 +66,11 @@
 #ifndef RS_MATCH_BITS
 #define RS_MATCH_BITS 3
 #endif
-#ifndef RS_BALLOT_XOR
-#define RS_BALLOT_XOR 1
-#endif
 #ifndef RS_LOOKBACK_BATCH
 #define RS_LOOKBACK_BATCH 4
 #endif
 #ifndef RS_TILE_MIN_THREADS_PER_SM
 #define RS_TILE_MIN_THREADS_PER_SM 1024
-#endif
-//   RS_CHAINS       each warp's segment is split into this many contiguous
-//                   parts with separate digit counters ("virtual warps"),
-//                   ranked interleaved: independent dependency chains.
-#ifndef RS_CHAINS
-#define RS_CHAINS 1
-#endif
-//   RS_RANK_ATOMIC  1: one leader lane per digit advances the counter with a
-//                   shared atomic and hands the old count to its peers with a
-//                   shuffle; 0: every lane reads the counter and the peers
-//                   store the advanced count.
-#ifndef RS_RANK_ATOMIC
-#define RS_RANK_ATOMIC 0
-#endif
-//   RS_LOAD_STREAM  1: tile loads are streaming (evict-first) loads.
-//   RS_STORE_KEEP   1: scatter stores carry an L2 evict-last policy, so lines
-//                   that a digit run leaves half written stay resident until
-//                   the next tile completes them.
-#ifndef RS_LOAD_STREAM
-#define RS_LOAD_STREAM 0
-#endif
-#ifndef RS_STORE_KEEP
-#define RS_STORE_KEEP 1
 #endif
 
 namespace rs {
@@ -321,14 +295,12 @@ template <typename T, int RB, int THREADS, int ITEMS, int VB>
 struct TileSmem {
     static constexpr int BINS = 1 << RB;
     static constexpr int WARPS = THREADS / 32;
-    static constexpr int CHAINS = (ITEMS % RS_CHAINS == 0) ? RS_CHAINS : 1;
-    static constexpr int VWARPS = WARPS * CHAINS;  // counter arrays ("virtual warps")
     static constexpr int TILE = THREADS * ITEMS;
     static constexpr int WH = BINS + 1;  // per-array counters + one dummy slot for tail lanes
     static constexpr size_t keys_off = 0;
     static constexpr size_t vals_off = align_up(sizeof(T) * TILE, 16);
     static constexpr size_t wh_off = vals_off + (VB ? align_up(sizeof(ValT<VB>) * (size_t)TILE, 16) : 0);
-    static constexpr size_t base_off = wh_off + align_up(4 * (size_t)VWARPS * WH, 16);
+    static constexpr size_t base_off = wh_off + align_up(4 * (size_t)WARPS * WH, 16);
     static constexpr size_t scan_off = base_off + 4 * BINS;
     static constexpr size_t misc_off = scan_off + 4 * 32;
     static constexpr size_t io_off = misc_off + 16;  // this pass's 4 buffer pointers
@@ -554,13 +526,8 @@ __device__ __forceinline__ void load_striped(const T* __restrict__ src, uint32_t
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
         const uint32_t i = seg + k * 32 + lane;
-#if RS_LOAD_STREAM
-        if (FULL) v[k] = __ldcs(src + i);
-        else v[k] = i < n ? __ldcs(src + i) : T(0);
-#else
         if (FULL) v[k] = src[i];
         else v[k] = i < n ? src[i] : T(0);
-#endif
     }
 }
 
@@ -658,11 +625,7 @@ __device__ __forceinline__ uint32_t warp_peers(uint32_t v)
     for (int b = 0; b < (BITS < BALLOT_BITS ? BITS : BALLOT_BITS); ++b) {
         const uint32_t bit = (v >> b) & 1u;
         const uint32_t bal = __ballot_sync(0xFFFFFFFFu, bit);
-#if RS_BALLOT_XOR
         peers &= bal ^ (bit - 1u);  // bit - 1 is all ones exactly when the bit is clear
-#else
-        peers &= bit ? bal : ~bal;
-#endif
     }
     return peers;
 }
@@ -683,37 +646,22 @@ __device__ __forceinline__ uint32_t step_digit(const typename KeyOps<KT>::T (&ke
     return (FULL || seg + k * 32 + lane < n) ? d : (1u << RB);
 }
 
-template <bool FULL, int KT, int RB, int ITEMS, int CHAINS, int WH>
+template <bool FULL, int KT, int RB, int ITEMS>
 __device__ __forceinline__ void rank_in_warp(const typename KeyOps<KT>::T (&key)[ITEMS], uint32_t seg,
                                              uint32_t n, uint32_t shift, uint32_t mask, uint32_t flip,
-                                             uint32_t* wh, int lane, uint32_t (&rank)[(ITEMS + 1) / 2])
+                                             uint32_t* cnt, int lane, uint32_t (&rank)[(ITEMS + 1) / 2])
 {
-    // Part c holds steps [c*L, (c+1)*L) and counts into wh + c*WH; the parts
-    // are visited interleaved (j-th step of every part, then the next j).
-    constexpr int L = ITEMS / CHAINS;
     const uint32_t lt = lanemask_lt();
 #pragma unroll
     for (int i = 0; i < (ITEMS + 1) / 2; ++i) rank[i] = 0;
 #pragma unroll
-    for (int j = 0; j < L; ++j) {
-#pragma unroll
-        for (int c = 0; c < CHAINS; ++c) {
-            const int k = c * L + j;
-            uint32_t* cnt = wh + c * WH;
-            const uint32_t d = step_digit<FULL, KT, RB, ITEMS>(key, k, seg, n, shift, mask, flip, lane);
-            const uint32_t peers = warp_peers<FULL ? RB : RB + 1, RB>(d);
-#if RS_RANK_ATOMIC
-            const int leader = 31 - __clz(peers);
-            uint32_t old = 0;
-            if (leader == lane) old = atomicAdd(cnt + d, (uint32_t)__popc(peers));
-            const uint32_t prior = __shfl_sync(0xFFFFFFFFu, old, leader);
-#else
-            const uint32_t prior = cnt[d];
-            cnt[d] = prior + __popc(peers);
-#endif
-            const uint32_t r = prior + __popc(peers & lt);
-            rank[k / 2] |= (k & 1) ? (r << 16) : r;
-        }
+    for (int k = 0; k < ITEMS; ++k) {
+        const uint32_t d = step_digit<FULL, KT, RB, ITEMS>(key, k, seg, n, shift, mask, flip, lane);
+        const uint32_t peers = warp_peers<FULL ? RB : RB + 1, RB>(d);
+        const uint32_t prior = cnt[d];
+        cnt[d] = prior + __popc(peers);
+        const uint32_t r = prior + __popc(peers & lt);
+        rank[k / 2] |= (k & 1) ? (r << 16) : r;
         __syncwarp();
     }
 }
@@ -723,7 +671,7 @@ template <typename S>
 __device__ __forceinline__ void zero_counters(unsigned char* smem, int threads)
 {
     uint32_t* whist = reinterpret_cast<uint32_t*>(smem + S::wh_off);
-    for (int i = threadIdx.x; i < S::VWARPS * S::WH; i += threads) whist[i] = 0;
+    for (int i = threadIdx.x; i < S::WARPS * S::WH; i += threads) whist[i] = 0;
 }
 
 // Everything of one tile, whose keys are in registers, up to the point where
@@ -743,7 +691,7 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
 {
     using T = typename KeyOps<KT>::T;
     using S = TileSmem<T, RB, THREADS, ITEMS, VB>;
-    constexpr int BINS = S::BINS, TILE = S::TILE, WH = S::WH, CHAINS = S::CHAINS, VWARPS = S::VWARPS;
+    constexpr int BINS = S::BINS, TILE = S::TILE, WH = S::WH, WARPS = S::WARPS;
     T* skeys = reinterpret_cast<T*>(smem + S::keys_off);
     ValT<VB>* svals = reinterpret_cast<ValT<VB>*>(smem + S::vals_off);
     uint32_t* whist = reinterpret_cast<uint32_t*>(smem + S::wh_off);
@@ -755,8 +703,7 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
 
     // (the caller has zeroed the counters and synchronised)
     uint32_t rank[(ITEMS + 1) / 2];
-    rank_in_warp<FULL, KT, RB, ITEMS, CHAINS, WH>(key, seg, p.n, p.shift, p.mask, p.flip,
-                                                  whist + warp * CHAINS * WH, lane, rank);
+    rank_in_warp<FULL, KT, RB, ITEMS>(key, seg, p.n, p.shift, p.mask, p.flip, whist + warp * WH, lane, rank);
     __syncthreads();
 
     // Per digit: the tile count, and after the scan each warp's start for the
@@ -765,14 +712,14 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
     uint32_t cnt = 0;
     if (tid < BINS) {
 #pragma unroll
-        for (int w = 0; w < VWARPS; ++w) cnt += whist[w * WH + tid];
+        for (int w = 0; w < WARPS; ++w) cnt += whist[w * WH + tid];
         publish(tid, cnt);
     }
     const uint32_t start = bins_exclusive_scan<BINS, false>(tid < BINS ? cnt : 0u, sscan + 16, nullptr);
     if (tid < BINS) {
         uint32_t run = start;
 #pragma unroll
-        for (int w = 0; w < VWARPS; ++w) {
+        for (int w = 0; w < WARPS; ++w) {
             const uint32_t c = whist[w * WH + tid];
             whist[w * WH + tid] = run;
             run += c;
@@ -783,12 +730,12 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
     // Shuffle: each digit becomes one contiguous run of the tile.  pos < TILE
     // holds by construction; the clamp keeps a violation inside the tile.
     uint32_t bad = 0;
-    const uint32_t* wbase = whist + warp * CHAINS * WH;
+    const uint32_t* wbase = whist + warp * WH;
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
         const uint32_t d = step_digit<FULL, KT, RB, ITEMS>(key, k, seg, p.n, p.shift, p.mask, p.flip, lane);
         const uint32_t r = (k & 1) ? (rank[k / 2] >> 16) : (rank[k / 2] & 0xFFFFu);
-        uint32_t pos = wbase[(k / (ITEMS / CHAINS)) * WH + d] + r;
+        uint32_t pos = wbase[d] + r;
 #if RS_CHECKED
         bad |= pos >= (uint32_t)TILE;
 #endif
@@ -821,9 +768,7 @@ __device__ __forceinline__ void tile_scatter(const PassParams& p, unsigned char*
     const uint32_t tile_base = tile * (uint32_t)TILE;
     const uint32_t valid = FULL ? (uint32_t)TILE : p.n - tile_base;
     uint32_t bad = 0;
-#if RS_STORE_KEEP
-    const uint64_t pol = l2_evict_last_policy();
-#endif
+    const uint64_t pol = l2_evict_last_policy();  // half-written lines stay until the next tile fills them
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
         const uint32_t s = (uint32_t)(k * THREADS) + threadIdx.x;
@@ -833,13 +778,8 @@ __device__ __forceinline__ void tile_scatter(const PassParams& p, unsigned char*
             const bool ok = idx < p.n;
             bad |= !ok;
             if (ok) {
-#if RS_STORE_KEEP
                 st_keep(out + idx, kk, pol);
                 if constexpr (VB != 0) st_keep(vout + idx, svals[s], pol);
-#else
-                out[idx] = kk;
-                if constexpr (VB != 0) vout[idx] = svals[s];
-#endif
             }
         }
     }
