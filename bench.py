@@ -32,7 +32,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "Gkeys/s sorted (32-bit keys, 2^28) on 1 GB300; % of HBM roofline"
-DEFAULT_WORKLOAD = "c4a_u32_2p28"
+DEFAULT_WORKLOAD = "u32_uniform_2p28"
 L2_BYTES = 126 * 2**20
 FALLBACK_HBM_GBS = 6800.0
 KIND_NAMES = {1: "histogram", 2: "onesweep_pass", 3: "upsweep", 4: "spine_scan", 5: "downsweep",

@@ -85,7 +85,7 @@ typedef enum rs_status {
     RS_ERR_CUDA = 4,           /* a CUDA runtime call failed                           */
     RS_ERR_DEVICE_TIMEOUT = 5, /* a look-back wait ran out (device error word)         */
     RS_ERR_CHECK_FAILED = 6,   /* a device bounds check failed (device error word)     */
-    RS_ERR_UNSUPPORTED = 7     /* valid request this build does not handle             */
+    RS_ERR_UNSUPPORTED = 7     /* valid request this library does not handle           */
 } rs_status;
 
 typedef enum rs_key_type {

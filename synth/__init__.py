@@ -182,6 +182,7 @@ class Workload:
     begin_bit: int
     end_bit: int
     seed: int
+    generator: str     # "uniform32" | "normal_specials32" | "morton30" | "and4" | "uniform64"
     description: str
 
     @property
@@ -191,20 +192,14 @@ class Workload:
     def keys(self, n: int | None = None, out=None):
         """Key bit patterns (uint32 or uint64 array); n overrides the size (prefix-stable)."""
         n = self.n if n is None else n
-        kind = self.name.split("_")[0]
-        if kind in ("c1", "c4a", "sweep"):
-            return u32_uniform(n, self.seed, out)
-        if kind == "c2":
-            return f32_normal_specials(n, self.seed, out=out)
-        if kind == "c3":
-            return u32_uniform(n, self.seed, out)          # int32 bit patterns, full range
-        if kind == "c4b":
-            return u32_morton30(n, self.seed, out)
-        if kind == "c4c":
-            return u32_and4(n, self.seed, out)
-        if kind == "c5":
-            return u64_uniform(n, self.seed, out)
-        raise KeyError(self.name)
+        gen = {"uniform32": lambda: u32_uniform(n, self.seed, out),
+               "normal_specials32": lambda: f32_normal_specials(n, self.seed, out=out),
+               "morton30": lambda: u32_morton30(n, self.seed, out),
+               "and4": lambda: u32_and4(n, self.seed, out),
+               "uniform64": lambda: u64_uniform(n, self.seed, out)}
+        if self.generator not in gen:
+            raise KeyError(self.generator)
+        return gen[self.generator]()
 
     def values(self, n: int | None = None, out=None):
         n = self.n if n is None else n
@@ -214,19 +209,19 @@ class Workload:
 WORKLOADS = {
     w.name: w
     for w in [
-        Workload("c1_u32_2p16", "u32", 16, False, 0, 32, 0x5EED0001,
+        Workload("u32_uniform_2p16", "u32", 16, False, 0, 32, 0x5EED0001, "uniform32",
                  "2^16 uint32 keys uniform over 32 bits, keys-only, bits [0,32)"),
-        Workload("c2_f32_2p24", "f32", 24, False, 0, 32, 0x5EED0002,
+        Workload("f32_normal_specials_2p24", "f32", 24, False, 0, 32, 0x5EED0002, "normal_specials32",
                  "2^24 float32 N(0,1) keys with 0.1% each of -0.0, +0.0, +Inf, -Inf, qNaN; keys-only"),
-        Workload("c3_i32_2p26", "i32", 26, True, 0, 32, 0x5EED0003,
+        Workload("i32_uniform_index_2p26", "i32", 26, True, 0, 32, 0x5EED0003, "uniform32",
                  "2^26 int32 keys uniform over the signed range, payload = index"),
-        Workload("c4a_u32_2p28", "u32", 28, False, 0, 32, 0x5EED0004,
+        Workload("u32_uniform_2p28", "u32", 28, False, 0, 32, 0x5EED0004, "uniform32",
                  "2^28 uint32 keys uniform over 32 bits, keys-only"),
-        Workload("c4b_morton_2p28", "u32", 28, True, 0, 30, 0x1_5EED0004,
+        Workload("morton30_index_2p28", "u32", 28, True, 0, 30, 0x1_5EED0004, "morton30",
                  "2^28 30-bit Morton codes of uniform 3-D points, payload = index, bits [0,30)"),
-        Workload("c4c_and4_2p28", "u32", 28, False, 0, 32, 0x2_5EED0004,
+        Workload("u32_and4_2p28", "u32", 28, False, 0, 32, 0x2_5EED0004, "and4",
                  "2^28 uint32 keys, each the AND of 4 uniform words (P(bit)=1/16), keys-only"),
-        Workload("c5_u64_2p28", "u64", 28, True, 0, 64, 0x5EED0005,
+        Workload("u64_uniform_index_2p28", "u64", 28, True, 0, 64, 0x5EED0005, "uniform64",
                  "2^28 uint64 keys uniform over 64 bits, payload = index, bits [0,64)"),
     ]
 }
@@ -235,4 +230,4 @@ WORKLOADS = {
 def sweep_workload(log2n: int) -> Workload:
     """Uniform uint32 keys-only at 2^log2n (the roofline-knee size sweep, 2^16..2^29)."""
     return Workload(f"sweep_u32_2p{log2n}", "u32", log2n, False, 0, 32,
-                    0x5EED0005 + (log2n << 32), f"2^{log2n} uint32 keys uniform, keys-only")
+                    0x5EED0005 + (log2n << 32), "uniform32", f"2^{log2n} uint32 keys uniform, keys-only")

@@ -45,11 +45,11 @@ def test_workload_full_size(name):
 
 
 def test_chained_scan_full_size():
-    run_workload(synth.WORKLOADS["c4a_u32_2p28"], algo="onesweep")
+    run_workload(synth.WORKLOADS["u32_uniform_2p28"], algo="onesweep")
 
 
 def test_chained_scan_pairs_full_size():
-    run_workload(synth.WORKLOADS["c4b_morton_2p28"], algo="onesweep")
+    run_workload(synth.WORKLOADS["morton30_index_2p28"], algo="onesweep")
 
 
 def test_sweep_largest_size():

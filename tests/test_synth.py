@@ -65,10 +65,10 @@ def test_f32_specials_injected():
 
 def test_workload_table():
     w = synth.WORKLOADS
-    assert w["c4a_u32_2p28"].n == 1 << 28 and not w["c4a_u32_2p28"].with_values
-    assert w["c4b_morton_2p28"].end_bit == 30 and w["c4b_morton_2p28"].with_values
-    assert w["c5_u64_2p28"].key_type == "u64"
-    small = w["c3_i32_2p26"].keys(n=1000)
+    assert w["u32_uniform_2p28"].n == 1 << 28 and not w["u32_uniform_2p28"].with_values
+    assert w["morton30_index_2p28"].end_bit == 30 and w["morton30_index_2p28"].with_values
+    assert w["u64_uniform_index_2p28"].key_type == "u64"
+    small = w["i32_uniform_index_2p26"].keys(n=1000)
     assert small.dtype == np.uint32 and small.size == 1000
     assert synth.sweep_workload(20).n == 1 << 20
 
