@@ -77,6 +77,10 @@
 extern "C" {
 #endif
 
+/* Largest n any sort accepts (2^32 - 2^16; positions and tile indices stay in
+ * 32 bits). */
+#define RS_MAX_N 4294901760u
+
 typedef enum rs_status {
     RS_OK = 0,
     RS_ERR_INVALID_ARG = 1,    /* null pointer, bad bit range, n too large, bad enum   */

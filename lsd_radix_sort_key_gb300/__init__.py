@@ -71,6 +71,7 @@ SIGNATURES = {
 }
 SIGNATURES["rs_sort_keys_u32_noalloc"] = (_i, [_vp, _vp, _sz, _i, _i, _vp])
 NOALLOC_MAX_N = 1 << 22
+MAX_N = (1 << 32) - (1 << 16)  # RS_MAX_N
 for _t in ("u32", "i32", "f32", "u64", "u16", "i16", "f16"):
     SIGNATURES[f"rs_sort_keys_{_t}"] = _KEYS_SIG
     SIGNATURES[f"rs_sort_pairs_{_t}"] = _PAIRS_SIG

@@ -24,7 +24,7 @@ extern template rs_status run_sort<KF16>(Plan& pl);
 
 namespace {
 
-constexpr size_t kMaxN = (size_t)0xFFFF0000u;        // 2^32 - 2^16
+constexpr size_t kMaxN = (size_t)RS_MAX_N;           // 2^32 - 2^16
 constexpr size_t kOnesweepMaxN = ((size_t)1 << 30) - 1;
 constexpr size_t kAutoReduceScanMinN = (size_t)1 << 25;
 constexpr uint32_t kDefaultSpinLimit = 1u << 20;      // each spin is one L2 round trip (~1 s in all)
