@@ -13,7 +13,7 @@
 //      and a scatter of the runs to global memory ("정렬: 라딕스와 머지소트",
 //      13.4: coalescing through shared memory).
 //
-// Two schedules are built from the same tile code:
+// Three schedules are built from the same tile code:
 //   * chained scan (k_histogram once, then k_onesweep per pass): every tile
 //     takes a ticket, publishes its digit counts, and looks back over its
 //     predecessors' published counts for its global offsets (decoupled
@@ -22,6 +22,15 @@
 //     once up front for all histograms.
 //   * reduce-then-scan (k_upsweep, k_spine_scan, k_downsweep per pass): each
 //     CTA owns a contiguous chunk of tiles; the spine scan is step 2 proper.
+//     Full tiles of keys-only 32/16-bit sorts reach shared memory by 1-D bulk
+//     copies (cp.async.bulk) one tile ahead.
+//   * small sorts (k_cluster_sort): the whole sort in one launch on a
+//     thread-block cluster whose CTAs keep their tiles in shared memory and
+//     exchange counts and keys through distributed shared memory.
+//
+// Keys may be 32-, 64- or 16-bit, values absent, 32- or 64-bit (VB = value
+// bytes), and the order ascending or descending (each digit XORed with its
+// mask).
 //
 // Pass skipping: the first read of the keys (k_histogram, or the first
 // k_upsweep) also records which key bits differ between keys and whether the
@@ -32,7 +41,8 @@
 // the result still lands in keys_out (section "pass skipping" below).
 //
 // Keys are carried with their original bit patterns.  The order-preserving
-// map T (identity, sign flip for int32, the NaN/Inf-aware flip for float32)
+// map T (identity, sign flip for int32/int16, the NaN/Inf-aware flip for
+// float32 and binary16)
 // is applied when a digit is extracted, in every pass -- as the CPU code of
 // "Radix sort を実装 & 測定してみた" (section 実装) does -- so no inverse map
 // is needed and NaN/Inf payloads come back unchanged.
@@ -732,7 +742,7 @@ __device__ __forceinline__ void zero_counters(unsigned char* smem, int threads)
 // the tile's count of digit d in *cnt and its tile-local start in *start.
 // `publish(d, cnt)` runs for every digit as soon as the count is known (the
 // chained scan publishes it there).  The key/value registers are free again
-// on return (the caller prefetches the next tile into them).
+// on return (the downsweep loads its next tile into them).
 template <bool FULL, int KT, int RB, int THREADS, int ITEMS, int VB, typename Publish>
 __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsigned char* smem,
                                                       uint32_t tile,
