@@ -93,10 +93,14 @@ def measured_peaks():
 
 
 def kernel_source_hash() -> str:
+    """sha256 (first 16 hex digits) of the files that define or instantiate
+    device code: the kernels, their shapes and the per-key-type translation
+    units.  The host entry layer (argument checks, schedule choice) is left
+    out: changing it changes no kernel."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "lsd_radix_sort_key_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh", ".h")):
+        if fn in ("rs_kernels.cuh", "rs_config.h") or (fn.startswith("rs_sort_") and fn.endswith(".cu")):
             with open(os.path.join(csrc, fn), "rb") as f:
                 h.update(fn.encode())
                 h.update(f.read())
