@@ -279,6 +279,33 @@ rs_status rs_sort_host(rs_key_type key_type, const void* h_keys_in, void* h_keys
                        int end_bit, void* d_work, size_t work_bytes, void* stream);
 
 /*
+ * End-to-end sort of a sequence of `batches` independent HOST batches of n
+ * keys each (same key type and bit range), pipelined: while batch i is
+ * sorted on the device, batch i+1 is copied in and batch i-1 copied out, so
+ * the host link carries both directions at once.  Batch i reads
+ * h_keys_in[i] (and h_vals_in[i]) and writes h_keys_out[i] (and
+ * h_vals_out[i]); each result is the same as rs_sort_host's for that batch.
+ * The pointer arrays are read during the call only; the host buffers must
+ * stay valid (and page-locked for full copy speed) until `stream`
+ * completes.  h_vals_in and h_vals_out are both NULL (keys only) or both
+ * arrays of non-NULL pointers.  d_work is a caller-owned device buffer of
+ * rs_host_batches_work_bytes(...) bytes (two slots of rs_host_work_bytes,
+ * used alternately).
+ * The work runs on three internal streams forked from and joined back into
+ * `stream` (also when an enqueue fails), so the call returns once the work
+ * is enqueued and the outputs are valid after `stream` completes.  Not
+ * capturable: RS_ERR_UNSUPPORTED while `stream` is capturing.  Errors:
+ * RS_ERR_INVALID_ARG (negative batches, a NULL pointer, a bad shape),
+ * RS_ERR_TEMP_TOO_SMALL, RS_ERR_CUDA.
+ */
+size_t rs_host_batches_work_bytes(rs_key_type key_type, int with_values, size_t n, int begin_bit,
+                                  int end_bit);
+rs_status rs_sort_host_batches(rs_key_type key_type, int batches, const void* const* h_keys_in,
+                               void* const* h_keys_out, const uint32_t* const* h_vals_in,
+                               uint32_t* const* h_vals_out, size_t n, int begin_bit, int end_bit,
+                               void* d_work, size_t work_bytes, void* stream);
+
+/*
  * Sort without any allocation.  The pages have no counterpart to this entry
  * point; it exists for callers that cannot allocate device memory where they
  * sort: code running while a stream capture in global mode is active (where

@@ -68,6 +68,8 @@ SIGNATURES = {
     "rs_graph_destroy": (None, [_vp]),
     "rs_host_work_bytes": (_sz, [_i, _i, _sz, _i, _i]),
     "rs_sort_host": (_i, [_i, _vp, _vp, _vp, _vp, _sz, _i, _i, _vp, _sz, _vp]),
+    "rs_host_batches_work_bytes": (_sz, [_i, _i, _sz, _i, _i]),
+    "rs_sort_host_batches": (_i, [_i, _i, _vp, _vp, _vp, _vp, _sz, _i, _i, _vp, _sz, _vp]),
 }
 SIGNATURES["rs_sort_keys_u32_noalloc"] = (_i, [_vp, _vp, _sz, _i, _i, _vp])
 NOALLOC_MAX_N = 1 << 22
@@ -223,6 +225,33 @@ def rs_sort_host(key_type, h_keys_in, h_keys_out, h_vals_in, h_vals_out, n, begi
     return lib().rs_sort_host(KEY_TYPES[key_type], _addr(h_keys_in), _addr(h_keys_out),
                               _addr(h_vals_in), _addr(h_vals_out), n, begin_bit, end_bit,
                               _addr(d_work), work_bytes, _stream(stream))
+
+
+def rs_host_batches_work_bytes(key_type: str, with_values: bool, n: int, begin_bit: int,
+                               end_bit: int) -> int:
+    return lib().rs_host_batches_work_bytes(KEY_TYPES[key_type], int(bool(with_values)), n,
+                                            begin_bit, end_bit)
+
+
+def _ptr_array(bufs):
+    """A C array of the buffers' addresses (None stays None)."""
+    if bufs is None:
+        return None
+    return (ctypes.c_void_p * len(bufs))(*[_addr(b) for b in bufs])
+
+
+def rs_sort_host_batches(key_type, h_keys_in, h_keys_out, h_vals_in, h_vals_out, n, begin_bit,
+                         end_bit, d_work, work_bytes, stream=None) -> int:
+    """h_keys_in / h_keys_out (and h_vals_* or None): equal-length lists of
+    host buffers, one per batch."""
+    batches = len(h_keys_in)
+    if len(h_keys_out) != batches or (h_vals_in is not None and len(h_vals_in) != batches) or \
+            (h_vals_out is not None and len(h_vals_out) != batches):
+        raise ValueError("every buffer list needs one entry per batch")
+    arrays = [_ptr_array(x) for x in (h_keys_in, h_keys_out, h_vals_in, h_vals_out)]  # alive until return
+    ptrs = [None if a is None else ctypes.addressof(a) for a in arrays]
+    return lib().rs_sort_host_batches(KEY_TYPES[key_type], batches, *ptrs, n, begin_bit, end_bit,
+                                      _addr(d_work), work_bytes, _stream(stream))
 
 
 class Graph:

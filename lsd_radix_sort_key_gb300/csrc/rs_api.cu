@@ -438,4 +438,133 @@ rs_status rs_sort_host(rs_key_type key_type, const void* h_keys_in, void* h_keys
     return RS_OK;
 }
 
+size_t rs_host_batches_work_bytes(rs_key_type key_type, int with_values, size_t n, int begin_bit,
+                                  int end_bit)
+{
+    const size_t one = rs_host_work_bytes(key_type, with_values, n, begin_bit, end_bit);
+    if (one == (size_t)-1 || one == 0) return one;
+    return 2 * rs::align_up(one, 256);
+}
+
+}  // extern "C"
+
+namespace {
+
+// The streams and events of one rs_sort_host_batches call.  Destroying them
+// while their work is still pending is allowed: CUDA releases them once the
+// work completes.
+struct BatchPipe {
+    cudaStream_t sh = nullptr, sc = nullptr, sd = nullptr;  // copies in, sorts, copies out
+    cudaEvent_t fork = nullptr, join = nullptr;
+    cudaEvent_t in_done[2] = {}, sort_done[2] = {}, out_done[2] = {};
+    bool create()
+    {
+        const unsigned sf = cudaStreamNonBlocking, ef = cudaEventDisableTiming;
+        if (cudaStreamCreateWithFlags(&sh, sf) != cudaSuccess || cudaStreamCreateWithFlags(&sc, sf) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&sd, sf) != cudaSuccess)
+            return false;
+        if (cudaEventCreateWithFlags(&fork, ef) != cudaSuccess || cudaEventCreateWithFlags(&join, ef) != cudaSuccess)
+            return false;
+        for (int s = 0; s < 2; ++s)
+            if (cudaEventCreateWithFlags(&in_done[s], ef) != cudaSuccess ||
+                cudaEventCreateWithFlags(&sort_done[s], ef) != cudaSuccess ||
+                cudaEventCreateWithFlags(&out_done[s], ef) != cudaSuccess)
+                return false;
+        return true;
+    }
+    ~BatchPipe()
+    {
+        for (cudaStream_t s : {sh, sc, sd})
+            if (s) cudaStreamDestroy(s);
+        for (cudaEvent_t e : {fork, join, in_done[0], in_done[1], sort_done[0], sort_done[1], out_done[0], out_done[1]})
+            if (e) cudaEventDestroy(e);
+    }
+};
+
+}  // namespace
+
+extern "C" {
+
+rs_status rs_sort_host_batches(rs_key_type key_type, int batches, const void* const* h_keys_in,
+                               void* const* h_keys_out, const uint32_t* const* h_vals_in,
+                               uint32_t* const* h_vals_out, size_t n, int begin_bit, int end_bit,
+                               void* d_work, size_t work_bytes, void* stream)
+{
+    rs_status st = check_shape(key_type, n, begin_bit, end_bit);
+    if (st != RS_OK) return st;
+    if (batches < 0 || (batches > 0 && (!h_keys_in || !h_keys_out))) return RS_ERR_INVALID_ARG;
+    const bool vals = h_vals_in || h_vals_out;
+    if (vals && (!h_vals_in || !h_vals_out)) return RS_ERR_INVALID_ARG;
+    for (int i = 0; i < batches; ++i)
+        if (!h_keys_in[i] || !h_keys_out[i] || (vals && (!h_vals_in[i] || !h_vals_out[i])))
+            return RS_ERR_INVALID_ARG;
+    if (n == 0 || batches == 0) return RS_OK;
+    if (!d_work) return RS_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return RS_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone) return RS_ERR_UNSUPPORTED;
+
+    size_t kin, kout, vin, vout;
+    const rs::TempLayout t = host_work_layout(key_type, vals, n, begin_bit, end_bit, &kin, &kout, &vin, &vout);
+    const size_t slot_bytes = rs::align_up(t.total, 256);
+    if (work_bytes < 2 * slot_bytes) return RS_ERR_TEMP_TOO_SMALL;
+    const size_t kb = n * key_bytes(key_type), vbytes = n * 4;
+    const size_t sort_temp = rs::temp_layout(key_bytes(key_type), vals ? 4 : 0, n, begin_bit, end_bit).total;
+
+    BatchPipe bp;
+    if (!bp.create()) return RS_ERR_CUDA;
+    if (cudaEventRecord(bp.fork, s) != cudaSuccess) return RS_ERR_CUDA;
+    for (cudaStream_t x : {bp.sh, bp.sc, bp.sd})
+        if (cudaStreamWaitEvent(x, bp.fork, 0) != cudaSuccess) return RS_ERR_CUDA;
+
+    // Batch i uses slot i % 2.  Its copy in waits for the sort of batch i-2
+    // (the slot's input buffer), its sort for its copy in and for the copy
+    // out of batch i-2 (the slot's output buffer and temp), its copy out for
+    // its sort.  Each wait is enqueued after the record it refers to and
+    // before that event is recorded again.
+    st = RS_OK;
+    for (int i = 0; i < batches && st == RS_OK; ++i) {
+        const int k = i & 1;
+        unsigned char* w = static_cast<unsigned char*>(d_work) + k * slot_bytes;
+        bool ok = true;
+        if (i >= 2) ok = ok && cudaStreamWaitEvent(bp.sh, bp.sort_done[k], 0) == cudaSuccess;
+        ok = ok && cudaMemcpyAsync(w + kin, h_keys_in[i], kb, cudaMemcpyHostToDevice, bp.sh) == cudaSuccess;
+        if (vals) ok = ok && cudaMemcpyAsync(w + vin, h_vals_in[i], vbytes, cudaMemcpyHostToDevice, bp.sh) == cudaSuccess;
+        ok = ok && cudaEventRecord(bp.in_done[k], bp.sh) == cudaSuccess;
+        ok = ok && cudaStreamWaitEvent(bp.sc, bp.in_done[k], 0) == cudaSuccess;
+        if (i >= 2) ok = ok && cudaStreamWaitEvent(bp.sc, bp.out_done[k], 0) == cudaSuccess;
+        if (!ok) { st = RS_ERR_CUDA; break; }
+        rs_sort_desc d{};
+        d.key_type = key_type;
+        d.keys_in = w + kin;
+        d.keys_out = w + kout;
+        d.vals_in = vals ? static_cast<const void*>(w + vin) : nullptr;
+        d.vals_out = vals ? static_cast<void*>(w + vout) : nullptr;
+        d.n = n;
+        d.begin_bit = begin_bit;
+        d.end_bit = end_bit;
+        d.temp = w;
+        d.temp_bytes = sort_temp;
+        d.stream = bp.sc;
+        st = rs_sort(&d);
+        if (st != RS_OK) break;
+        ok = cudaEventRecord(bp.sort_done[k], bp.sc) == cudaSuccess;
+        ok = ok && cudaStreamWaitEvent(bp.sd, bp.sort_done[k], 0) == cudaSuccess;
+        ok = ok && cudaMemcpyAsync(h_keys_out[i], w + kout, kb, cudaMemcpyDeviceToHost, bp.sd) == cudaSuccess;
+        if (vals) ok = ok && cudaMemcpyAsync(h_vals_out[i], w + vout, vbytes, cudaMemcpyDeviceToHost, bp.sd) == cudaSuccess;
+        ok = ok && cudaEventRecord(bp.out_done[k], bp.sd) == cudaSuccess;
+        if (!ok) st = RS_ERR_CUDA;
+    }
+    // Join everything enqueued so far back into the caller's stream, also on
+    // an error, so that a sync of `stream` covers it.
+    bool joined = true;
+    for (cudaStream_t x : {bp.sh, bp.sc, bp.sd}) {
+        joined = joined && cudaEventRecord(bp.join, x) == cudaSuccess &&
+                 cudaStreamWaitEvent(s, bp.join, 0) == cudaSuccess;
+    }
+    if (!joined && st == RS_OK) st = RS_ERR_CUDA;
+    return st;
+}
+
 }  // extern "C"

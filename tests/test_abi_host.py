@@ -165,6 +165,29 @@ def test_64bit_values_shape_and_checks(lib):
                                    value_bytes=8)) == 2
 
 
+def test_host_batches_shape_and_checks(lib):
+    n = 1000
+    assert rs.rs_host_batches_work_bytes("u32", False, n, 0, 32) >= 2 * rs.rs_host_work_bytes("u32", False, n, 0, 32)
+    assert rs.rs_host_batches_work_bytes("u32", False, n, 0, 40) == 2**64 - 1   # bad bit range
+    assert rs.rs_host_batches_work_bytes("u32", False, 0, 0, 32) == 0
+    wb = rs.rs_host_batches_work_bytes("u32", True, n, 0, 32)
+    ins, outs = [FAKE, 2 * FAKE], [3 * FAKE, 4 * FAKE]
+    vin, vout = [5 * FAKE, 6 * FAKE], [7 * FAKE, 8 * FAKE]
+
+    def call(k_in=ins, k_out=outs, v_in=vin, v_out=vout, n=n, work=9 * FAKE, wbytes=wb, e=32):
+        return rs.rs_sort_host_batches("u32", k_in, k_out, v_in, v_out, n, 0, e, work, wbytes, 0)
+    assert call(e=33) == 1                                   # bad bit range
+    assert call(k_out=[3 * FAKE, None]) == 1                 # a NULL output
+    assert call(v_in=[5 * FAKE, None]) == 1                  # a NULL value input
+    assert call(v_out=None) == 1                             # values in but not out
+    assert call(work=None) == 1                              # no work buffer
+    assert call(k_in=[], k_out=[], v_in=[], v_out=[]) == 0   # no batches: nothing to do
+    assert call(n=0) == 0                                    # empty batches: nothing to do
+    assert lib.rs_sort_host_batches(0, -1, None, None, None, None, n, 0, 32, FAKE, wb, None) == 1
+    with pytest.raises(ValueError):
+        call(k_out=[3 * FAKE])
+
+
 def test_status_strings(lib):
     for code in range(8):
         assert rs.rs_status_string(code)

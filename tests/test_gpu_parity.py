@@ -258,6 +258,41 @@ def test_host_buffer_entry_point():
     assert np.array_equal(hvo.numpy().view(np.uint32), ref_v)
 
 
+@pytest.mark.parametrize("kt,with_vals,batches", [("u32", False, 5), ("f32", True, 4), ("u64", True, 1),
+                                                  ("i32", False, 2)])
+def test_host_batches_entry_point(kt, with_vals, batches):
+    """Pipelined host batches: every batch (distinct keys, both slots reused,
+    an odd count ending in slot 0) equals the oracle's sort of it."""
+    n = 150_001
+    gen = {"u32": synth.u32_uniform, "i32": synth.u32_uniform, "f32": synth.f32_edge,
+           "u64": synth.u64_uniform}[kt]
+    keys = [gen(n, 80 + i) for i in range(batches)]
+    vals = [synth.u32_uniform(n, 90 + i) for i in range(batches)] if with_vals else None
+    pin = lambda a: torch.from_numpy(a.view(np.int64 if a.dtype == np.uint64 else np.int32)).pin_memory()
+    hk = [pin(k) for k in keys]
+    hko = [torch.empty_like(h).pin_memory() for h in hk]
+    hv = [pin(v) for v in vals] if with_vals else None
+    hvo = [torch.empty_like(h).pin_memory() for h in hv] if with_vals else None
+    bits = rs.KEY_BITS[kt]
+    wb = rs.rs_host_batches_work_bytes(kt, with_vals, n, 0, bits)
+    work = torch.empty(wb, dtype=torch.uint8, device="cuda:0")
+    stream = torch.cuda.Stream()
+    assert rs.rs_sort_host_batches(kt, hk, hko, hv, hvo, n, 0, bits, work, wb, stream) == 0
+    stream.synchronize()
+    udt = np.uint64 if kt == "u64" else np.uint32
+    for i in range(batches):
+        ref_k, ref_v = oracle.sort(kt, keys[i], vals[i] if with_vals else None, 0, bits)
+        assert np.array_equal(hko[i].numpy().view(udt), ref_k), f"batch {i} keys"
+        if with_vals:
+            assert np.array_equal(hvo[i].numpy().view(np.uint32), ref_v), f"batch {i} values"
+    # too small a work buffer, and a capturing stream, are refused before any work
+    assert rs.rs_sort_host_batches(kt, hk, hko, hv, hvo, n, 0, bits, work, wb - 1, stream) == 2
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        code = rs.rs_sort_host_batches(kt, hk, hko, hv, hvo, n, 0, bits, work, wb, stream)
+    assert code == 7  # RS_ERR_UNSUPPORTED
+
+
 def test_lookback_timeout_is_reported_and_recoverable():
     """Tile 3 never publishes: the waits behind it run out after a short bound,
     the sort reports RS_ERR_DEVICE_TIMEOUT, and the next sort is correct."""
