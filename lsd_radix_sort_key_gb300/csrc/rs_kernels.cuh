@@ -277,6 +277,17 @@ __device__ __forceinline__ uint32_t lanemask_lt()
 // so a root cause (a timed-out wait) is never hidden by its consequences.
 __device__ __forceinline__ void record_error(uint32_t* err, uint32_t code) { atomicOr(err, 1u << code); }
 
+// Programmatic dependent launch: every kernel of a sort after its first is
+// launched as a dependent of the kernel before it in the stream, so its CTAs
+// are set up as that kernel's last CTAs exit instead of after a full launch
+// round trip.  wait_prior_grid() blocks until the kernel before has completed
+// and its writes are visible (every earlier kernel completed before that one
+// passed its own wait); it returns at once after a plain launch.  A kernel
+// touches no global memory before its wait.  (The kernels do not signal
+// their dependents early: measured on GB300, letting the next kernel's CTAs
+// in while a kernel still runs was slower in graph replays.)
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Exclusive scan of one value per digit over the first BINS threads of the
 // block (others pass 0).  Every thread must call it: it holds one barrier, and
 // a second one unless TRAILING_SYNC is false.  `scratch` needs (BINS + 31) / 32
@@ -976,6 +987,8 @@ __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS)
     uint32_t* smisc = reinterpret_cast<uint32_t*>(smem + S::misc_off);
     const int tid = threadIdx.x;
     RoleShared* rsh = reinterpret_cast<RoleShared*>(smisc + 1);
+    zero_counters<S>(smem, THREADS);
+    wait_prior_grid();
     if (tid == 0) {
         // The skip record is read and the ticket taken together, so the two
         // round trips overlap (a skipped pass leaves its tickets unused).
@@ -989,7 +1002,6 @@ __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS)
             set_pass_io<S>(smem, q);
         }
     }
-    zero_counters<S>(smem, THREADS);
     __syncthreads();
     const PassRole role = read_role(rsh);
     if (!role.run) {
@@ -1026,16 +1038,18 @@ __global__ void __launch_bounds__(THREADS) k_upsweep(PassParams p)
     __shared__ uint32_t hist[BINS * COLS];
     __shared__ RoleShared rsh;
     __shared__ uint32_t skip_blk[3];
-    if constexpr (!FIRST) {
-        const PassRole role = block_pass_role(p, &rsh);
-        if (!role.run) return;
-        pass_buffers<false>(p, role);
-    }
     const int tid = threadIdx.x, lane = tid & 31;
     const uint32_t col = lane;
     for (int i = tid; i < BINS * COLS; i += THREADS) hist[i] = 0;
     if (FIRST && tid < 3) skip_blk[tid] = 0;
-    __syncthreads();
+    wait_prior_grid();
+    if constexpr (!FIRST) {
+        const PassRole role = block_pass_role(p, &rsh);  // (its barrier also covers the zeroing)
+        if (!role.run) return;
+        pass_buffers<false>(p, role);
+    } else {
+        __syncthreads();
+    }
     const uint32_t g = blockIdx.x;
     const uint64_t lo64 = (uint64_t)g * p.tiles_per_cta * TILE;
     const uint32_t lo = lo64 < p.n ? (uint32_t)lo64 : p.n;
@@ -1122,22 +1136,31 @@ __global__ void __launch_bounds__(THREADS) k_upsweep(PassParams p)
 template <int RB, int THREADS>
 __global__ void __launch_bounds__(THREADS) k_spine_scan(PassParams p, uint32_t* row_total)
 {
+    // Each thread owns PER consecutive counts (G <= kRtsMaxCtas): all its
+    // loads are issued at once, together with the plan read, so the kernel
+    // pays about one memory latency before the scan and one after.
+    constexpr uint32_t PER = (kRtsMaxCtas + THREADS - 1) / THREADS;
     __shared__ uint32_t sscan[32];
     __shared__ RoleShared rsh;
-    if (!block_pass_role(p, &rsh).run) return;
     const int tid = threadIdx.x;
     const uint32_t G = p.G;
     uint32_t* row = p.counts + (size_t)blockIdx.x * G;
     const uint32_t per = (G + THREADS - 1) / THREADS;
     const uint32_t lo = min(G, tid * per), hi = min(G, lo + per);
+    wait_prior_grid();
+    uint32_t c[PER];
+#pragma unroll
+    for (uint32_t j = 0; j < PER; ++j) c[j] = lo + j < hi ? row[lo + j] : 0u;
+    if (!block_pass_role(p, &rsh).run) return;  // (a skipped pass's counts are stale, unused)
     uint32_t sum = 0;
-    for (uint32_t i = lo; i < hi; ++i) sum += row[i];
+#pragma unroll
+    for (uint32_t j = 0; j < PER; ++j) sum += c[j];
     uint32_t total;
     uint32_t run = bins_exclusive_scan<THREADS>(sum, sscan, &total);
-    for (uint32_t i = lo; i < hi; ++i) {
-        const uint32_t c = row[i];
-        row[i] = run;
-        run += c;
+#pragma unroll
+    for (uint32_t j = 0; j < PER; ++j) {
+        if (lo + j < hi) row[lo + j] = run;
+        run += c[j];
     }
     if (tid == 0) row_total[blockIdx.x] = total;
 }
@@ -1268,6 +1291,8 @@ __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS)
     RoleShared* rsh = reinterpret_cast<RoleShared*>(smem + S::misc_off + 4);
     const int tid = threadIdx.x;
     const uint32_t g = blockIdx.x;
+    zero_counters<S>(smem, THREADS);
+    wait_prior_grid();
     // This CTA's digit totals and block offsets are read while thread 0
     // reads the skip record (for a skipped pass they are dropped).
     const uint32_t total = tid < BINS ? p.ghist[tid] : 0u;
@@ -1281,7 +1306,6 @@ __global__ void __launch_bounds__(THREADS, RS_TILE_MIN_THREADS_PER_SM / THREADS)
             set_pass_io<S>(smem, q);
         }
     }
-    zero_counters<S>(smem, THREADS);
     // The scan's barriers also publish the role, the PassIO slots and the zeroed counters.
     const uint32_t dstart = bins_exclusive_scan<BINS>(total, sscan, nullptr);
     const PassRole role = read_role(rsh);
@@ -1317,6 +1341,7 @@ template <int RB, typename T, int VB>
 __global__ void __launch_bounds__(256) k_chain_copy(PassParams p)
 {
     __shared__ RoleShared rsh;
+    wait_prior_grid();
     const PassRole role = block_pass_role(p, &rsh);
     if (p.in_place == 0u || role.E % 2u == 0u) return;
     copy_span<T, VB>(static_cast<const T*>(p.alt_keys), static_cast<T*>(p.sort_keys_out), p.alt_vals,
@@ -1694,6 +1719,7 @@ struct Plan {
     int* kinds;
     bool count_only;   // only count kernels, launch nothing
     bool auto_chosen;  // the schedule came from RS_ALGO_AUTO
+    bool launch_failed = false;
 };
 
 enum KernelKind { kKindHistogram = 1, kKindOnesweep = 2, kKindUpsweep = 3, kKindSpine = 4,
@@ -1703,13 +1729,35 @@ enum KernelKind { kKindHistogram = 1, kKindOnesweep = 2, kKindUpsweep = 3, kKind
 inline rs_status after_launch(Plan& pl, int kind)
 {
     if (pl.count_only) { pl.launched++; return RS_OK; }
-    if (cudaGetLastError() != cudaSuccess) return RS_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess || pl.launch_failed) return RS_ERR_CUDA;
     if (pl.kinds && pl.launched < pl.max_events) pl.kinds[pl.launched] = kind;
     pl.launched++;
     if (pl.events && pl.launched < pl.max_events)
         if (cudaEventRecordWithFlags(pl.events[pl.launched], pl.stream, pl.event_flags) != cudaSuccess)
             return RS_ERR_CUDA;
     return RS_OK;
+}
+
+// Launch `kernel` on the plan's stream (nothing when only counting).  With
+// `dependent`, as a programmatic dependent of the kernel before it in the
+// stream (see wait_prior_grid); the first kernel of a sort is launched
+// plainly, so it waits for everything the caller enqueued before the sort.
+template <typename... KArgs, typename... Args>
+inline void launch(Plan& pl, bool dependent, void (*kernel)(KArgs...), unsigned grid, unsigned block,
+                   size_t smem, Args... args)
+{
+    if (pl.count_only) return;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = pl.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = dependent ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, kernel, args...) != cudaSuccess) pl.launch_failed = true;
 }
 
 inline int device_sm_count()
@@ -1795,7 +1843,7 @@ rs_status run_passes(Plan& pl)
     // In place, a final copy (k_chain_copy) runs when an odd number of passes ran.
     auto finish = [&]() -> rs_status {
         if (!in_place) return RS_OK;
-        if (!pl.count_only) k_chain_copy<RB, T, VB><<<4 * sms, 256, 0, pl.stream>>>(base);
+        launch(pl, true, k_chain_copy<RB, T, VB>, 4 * sms, 256, 0, base);
         return after_launch(pl, kKindCopy);
     };
 
@@ -1830,7 +1878,7 @@ rs_status run_passes(Plan& pl)
         const int hgrid = (int)std::max<size_t>(1, std::min<size_t>(want, (size_t)sms));
         const size_t hsmem = (size_t)P * BINS * HCOLS * 4;
         if (!pl.count_only && !set_smem(hk, hsmem)) return RS_ERR_CUDA;
-        if (!pl.count_only) hk<<<hgrid, 1024, hsmem, pl.stream>>>(h);
+        launch(pl, false, hk, hgrid, 1024, hsmem, h);
         rs_status st = after_launch(pl, kKindHistogram);
         if (st != RS_OK) return st;
         for (int q = 0; q < P; ++q) {
@@ -1840,13 +1888,12 @@ rs_status run_passes(Plan& pl)
             pp.shift = pl.begin_bit + q * RB;
             const uint32_t width = std::min(RB, pl.end_bit - (int)pp.shift);
             pp.mask = (1u << width) - 1u;
-        pp.flip = pl.descending ? pp.mask : 0u;
             pp.flip = pl.descending ? pp.mask : 0u;
             pp.status = big + (size_t)q * num_tiles * BINS;
             pp.ghist = meta + kGhistBase + q * BINS;
             pp.ticket = meta + kTicketBase + q;
             const bool byte_digit = (RB == 8) && (pp.shift % 8 == 0) && (pp.mask == 0xFFu) && !pl.descending;
-            if (!pl.count_only) (byte_digit ? pkb : pk)<<<num_tiles, THREADS, S::bytes, pl.stream>>>(pp);
+            launch(pl, true, byte_digit ? pkb : pk, num_tiles, THREADS, S::bytes, pp);
             st = after_launch(pl, kKindOnesweep);
             if (st != RS_OK) return st;
         }
@@ -1887,15 +1934,15 @@ rs_status run_passes(Plan& pl)
         pp.counts = big;
         pp.G = G;
         pp.tiles_per_cta = tpc;
-        if (!pl.count_only) (q == 0 ? uk0 : uk)<<<G, 512, 0, pl.stream>>>(pp);
+        launch(pl, q != 0, q == 0 ? uk0 : uk, G, 512, 0, pp);
         rs_status st = after_launch(pl, kKindUpsweep);
         if (st != RS_OK) return st;
         pp.ghist = meta + kGhistBase + q * BINS;  // row totals of this pass
-        if (!pl.count_only) k_spine_scan<RB, 256><<<BINS, 256, 0, pl.stream>>>(pp, meta + kGhistBase + q * BINS);
+        launch(pl, true, k_spine_scan<RB, 256>, BINS, 256, 0, pp, meta + kGhistBase + q * BINS);
         st = after_launch(pl, kKindSpine);
         if (st != RS_OK) return st;
         const bool byte_digit = (RB == 8) && (pp.shift % 8 == 0) && (pp.mask == 0xFFu) && !pl.descending;
-        if (!pl.count_only) (byte_digit ? dkb : dk)<<<G, THREADS, DSMEM, pl.stream>>>(pp);
+        launch(pl, true, byte_digit ? dkb : dk, G, THREADS, DSMEM, pp);
         st = after_launch(pl, kKindDownsweep);
         if (st != RS_OK) return st;
     }
