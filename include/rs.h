@@ -99,7 +99,7 @@ typedef enum rs_key_type {
 
 typedef enum rs_algo {
     RS_ALGO_AUTO = 0,        /* the cluster sort for n <= rs_cluster_max_n(),
-                                reduce-then-scan for n >= 2^24, the chained scan
+                                reduce-then-scan for n >= 2^22, the chained scan
                                 between (measured on GB300)                      */
     RS_ALGO_ONESWEEP = 1,    /* one upfront histogram read + one kernel per pass    */
     RS_ALGO_REDUCE_SCAN = 2, /* upsweep + spine scan + downsweep per pass           */

@@ -26,7 +26,7 @@ namespace {
 
 constexpr size_t kMaxN = (size_t)RS_MAX_N;           // 2^32 - 2^16
 constexpr size_t kOnesweepMaxN = ((size_t)1 << 30) - 1;
-constexpr size_t kAutoReduceScanMinN = (size_t)1 << 24;
+constexpr size_t kAutoReduceScanMinN = (size_t)1 << 22;
 constexpr uint32_t kDefaultSpinLimit = 1u << 20;      // each spin is one L2 round trip (~1 s in all)
 
 int key_bytes(rs_key_type kt) { return kt == RS_U64 ? 8 : kt >= RS_U16 ? 2 : 4; }
@@ -82,10 +82,11 @@ rs_status make_plan(const rs_sort_desc* d, rs::Plan* pl)
     const size_t cluster_max = rs::cluster_max_n(kb, vb);
     if (pl->algo == RS_ALGO_AUTO) {
         // Chosen by measurement on GB300: one cluster kernel while the keys fit
-        // in the cluster's shared memory; reduce-then-scan from 2^24 keys (at
-        // 2^24 it beats the chained scan host-launched and graph-replayed;
-        // at 2^23 the chained scan's 5 launches still win host-launched); the
-        // chained scan between.  The chained scan needs n < 2^30.
+        // in the cluster's shared memory; reduce-then-scan from 2^22 keys (from
+        // there on it beats the chained scan host-launched and graph-replayed,
+        // its 12 kernels' launches hidden by programmatic dependent launch; at
+        // 2^21 the chained scan's 5 kernels still win); the chained scan
+        // between.  The chained scan needs n < 2^30.
         const bool rts = n > kOnesweepMaxN || n >= kAutoReduceScanMinN;
         pl->algo = n <= cluster_max ? RS_ALGO_CLUSTER : rts ? RS_ALGO_REDUCE_SCAN : RS_ALGO_ONESWEEP;
         pl->auto_chosen = true;

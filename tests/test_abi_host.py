@@ -63,10 +63,10 @@ def test_kernel_counts(lib):
     assert count("u32", 1 << 20, 0, 32, "reduce_scan") == 3 * 4
     assert count("u32", 1 << 20, 7, 7, "onesweep") == 0
     assert count("u32", 0, 0, 32, "onesweep") == 0
-    # AUTO: chained scan below 2^24 keys, reduce-then-scan from there on
+    # AUTO: chained scan below 2^22 keys, reduce-then-scan from there on
     assert count("u32", 1 << 20, 0, 32, "auto") == 5
-    assert count("u64", (1 << 24) - 1, 0, 64, "auto", vals=True) == 9
-    assert count("u64", 1 << 24, 0, 64, "auto", vals=True) == 24
+    assert count("u64", (1 << 22) - 1, 0, 64, "auto", vals=True) == 9
+    assert count("u64", 1 << 22, 0, 64, "auto", vals=True) == 24
     assert count("u32", 1 << 26, 0, 32, "auto") == 12
     assert count("u32", 1 << 26, 0, 32, "auto", vals=True) == 12
     assert count("u64", 1 << 26, 0, 64, "auto") == 24
