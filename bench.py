@@ -124,6 +124,43 @@ def ncu_traffic(kind: str, workload: str):
     return entry.get("dram_bytes_per_launch")
 
 
+def link_times(host_in, host_out, dev_buf, dev) -> dict:
+    """The host link on this machine, for reading e2e: one step's input copied
+    in alone, its result copied out alone, and both at once on two streams
+    (best of 3, CUDA events).  The pipelined e2e step cannot beat `both_ms`."""
+    import torch
+    nbytes = host_in.numel() * host_in.element_size()
+    d_in = dev_buf[:nbytes].view(host_in.dtype)
+    d_out = dev_buf[nbytes:2 * nbytes].view(host_in.dtype)
+    side = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+
+    def best(fn):
+        ms = []
+        for _ in range(3):
+            cur = torch.cuda.current_stream(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(cur)
+            fn(cur)
+            e1.record(cur)
+            torch.cuda.synchronize(dev)
+            ms.append(e0.elapsed_time(e1))
+        return round(min(ms), 3)
+
+    def both(cur):
+        for sd in side:
+            sd.wait_stream(cur)
+        with torch.cuda.stream(side[0]):
+            d_in.copy_(host_in, non_blocking=True)
+        with torch.cuda.stream(side[1]):
+            host_out.copy_(d_out, non_blocking=True)
+        for sd in side:
+            cur.wait_stream(sd)
+    return {"bytes": nbytes,
+            "h2d_ms": best(lambda cur: d_in.copy_(host_in, non_blocking=True)),
+            "d2h_ms": best(lambda cur: host_out.copy_(d_out, non_blocking=True)),
+            "both_ms": best(both)}
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -479,7 +516,7 @@ def run_ours(args):
                        "d2h_bytes_per_step": n * (kbytes + vbytes),
                        "ms_per_step": round(pipe_ms, 3), "steps": e2e_steps,
                        "api": "rs_sort_host_batches (pinned host buffers, one batch per step, pipelined)",
-                       "serial": serial}
+                       "serial": serial, "link": link_times(host_k, outs_k[0], work2, dev)}
         del work2
 
     if rank == 0 and not args.no_cpu:
