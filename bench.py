@@ -96,18 +96,43 @@ def measured_peaks():
 
 
 def kernel_source_hash() -> str:
-    """sha256 (first 16 hex digits) of the files that define or instantiate
-    device code: the kernels, their shapes and the per-key-type translation
-    units.  The host entry layer (argument checks, schedule choice) is left
-    out: changing it changes no kernel."""
+    """sha256 (first 16 hex digits) of the code, without comments, of the
+    files that define or instantiate device code: the kernels, their shapes
+    and the per-key-type translation units.  The host entry layer (argument
+    checks, schedule choice) is left out: changing it changes no kernel."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "lsd_radix_sort_key_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
         if fn in ("rs_kernels.cuh", "rs_config.h") or (fn.startswith("rs_sort_") and fn.endswith(".cu")):
-            with open(os.path.join(csrc, fn), "rb") as f:
+            with open(os.path.join(csrc, fn), encoding="utf-8") as f:
                 h.update(fn.encode())
-                h.update(f.read())
+                h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
+
+
+def code_only(text: str) -> str:
+    """C/C++ source without comments and with whitespace collapsed, so that
+    the source hash changes with the code and not with its comments."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":  # string or character literal, kept whole
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
 
 
 def ncu_traffic(kind: str, workload: str):

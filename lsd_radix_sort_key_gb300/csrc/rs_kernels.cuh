@@ -32,6 +32,10 @@
 // bytes), and the order ascending or descending (each digit XORed with its
 // mask).
 //
+// The kernels of one sort are chained by programmatic dependent launch: every
+// kernel after the first waits on the device (griddepcontrol.wait) for the
+// one before it, so their launches overlap the previous kernel's drain.
+//
 // Pass skipping: the first read of the keys (k_histogram, or the first
 // k_upsweep) also records which key bits differ between keys and whether the
 // input is already in order, and its last CTA turns that into a plan of
@@ -42,10 +46,10 @@
 //
 // Keys are carried with their original bit patterns.  The order-preserving
 // map T (identity, sign flip for int32/int16, the NaN/Inf-aware flip for
-// float32 and binary16)
-// is applied when a digit is extracted, in every pass -- as the CPU code of
-// "Radix sort を実装 & 測定してみた" (section 実装) does -- so no inverse map
-// is needed and NaN/Inf payloads come back unchanged.
+// float32 and binary16) is applied when a digit is extracted, in every pass
+// -- as the CPU code of "Radix sort を実装 & 測定してみた" (section 実装)
+// does -- so no inverse map is needed and NaN/Inf payloads come back
+// unchanged.
 #pragma once
 
 #include <cooperative_groups.h>
