@@ -1494,11 +1494,14 @@ __global__ void __launch_bounds__(THREADS, 1) k_cluster_sort(ClusterParams cp)
     cluster.sync();  // every CTA's share is complete
     if (tid == 0) {
         uint32_t d_lo = 0, d_hi = 0, un = 0;
-        for (uint32_t r = 0; r < C; ++r) {
-            const uint32_t* rr = cluster.map_shared_rank(rec, r);
-            d_lo |= rr[0];
-            d_hi |= rr[1];
-            un |= rr[2];
+#pragma unroll
+        for (uint32_t r = 0; r < (uint32_t)kClusterMaxCtas; ++r) {
+            if (r < C) {
+                const uint32_t* rr = cluster.map_shared_rank(rec, r);
+                d_lo |= rr[0];
+                d_hi |= rr[1];
+                un |= rr[2];
+            }
         }
         uint32_t words[kMaxPasses];
         write_plan<RB>(d_lo, d_hi, un, words, cp.passes, cp.begin_bit, cp.end_bit);
@@ -1550,10 +1553,16 @@ __global__ void __launch_bounds__(THREADS, 1) k_cluster_sort(ClusterParams cp)
         cluster.sync();
         uint32_t tot = 0, before = 0;
         if (tid < BINS) {
-            for (uint32_t r = 0; r < C; ++r) {
-                const uint32_t x = *cluster.map_shared_rank(cnts + tid, r);
-                tot += x;
-                before += r < c ? x : 0u;
+            // All C remote reads are issued before any is summed (unrolled to
+            // the largest cluster), so they cost one round trip, not C.
+            uint32_t x[kClusterMaxCtas];
+#pragma unroll
+            for (uint32_t r = 0; r < (uint32_t)kClusterMaxCtas; ++r)
+                x[r] = r < C ? *cluster.map_shared_rank(cnts + tid, r) : 0u;
+#pragma unroll
+            for (uint32_t r = 0; r < (uint32_t)kClusterMaxCtas; ++r) {
+                tot += x[r];
+                before += r < c ? x[r] : 0u;
             }
         }
         const uint32_t dstart = bins_exclusive_scan<BINS>(tid < BINS ? tot : 0u, sscan, nullptr);
