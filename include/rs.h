@@ -57,7 +57,11 @@
  *   Stream.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
  *     default stream).  Calls only enqueue work: they do not synchronise,
  *     allocate or read device memory back, so they may be captured into a
- *     CUDA graph.  RS_OK means "enqueued"; faults the device detects (a
+ *     CUDA graph.  Inside one sort, every kernel after the first is launched
+ *     as a programmatic dependent of the kernel before it (it waits on the
+ *     device before touching memory); the first is an ordinary launch, so
+ *     the sort starts after the work enqueued before it, and ordinary work
+ *     enqueued after it starts after the sort's last kernel has finished.  RS_OK means "enqueued"; faults the device detects (a
  *     look-back wait that ran out, an index that failed its bounds check) are
  *     written to an error word inside `temp` and read by rs_device_status().
  *   Sizes.  n may be 0 (nothing is launched).  n must be at most
