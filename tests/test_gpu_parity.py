@@ -258,6 +258,7 @@ def test_host_buffer_entry_point():
     assert np.array_equal(hvo.numpy().view(np.uint32), ref_v)
 
 
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")  # the refused capture records nothing
 @pytest.mark.parametrize("kt,with_vals,batches", [("u32", False, 5), ("f32", True, 4), ("u64", True, 1),
                                                   ("i32", False, 2)])
 def test_host_batches_entry_point(kt, with_vals, batches):
