@@ -58,3 +58,26 @@ def test_committed_traffic_records_are_well_formed():
         assert kind and workload
         assert isinstance(v["dram_bytes_per_launch"], int) and v["dram_bytes_per_launch"] > 0
         assert len(v["source_hash"]) == 16
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` (the CPU oracle timed as the reference
+    arm) prints one JSON line with the contract's keys; a 2^16-key workload
+    keeps it quick."""
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "u32_uniform_2p16", "--steps", "2", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=300, cwd=bench.ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0 and line["steps"] == 2
+    assert line["config"]["workload"] == "u32_uniform_2p16"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
