@@ -182,3 +182,24 @@ def test_graph_replays_follow_the_data():
             assert rs.rs_skip_record(temp, stream)[1:] == expected_record("u32", keys, 0, 32)
     finally:
         g.close()
+
+
+# Large enough that every reduce-then-scan CTA walks several tiles (more
+# tiles than CTAs), so the running passes take their buffers from the plan
+# through several tile iterations: keys only (staged tiles) and with values,
+# in place and out of place, ascending and descending.
+N_MULTI = (1 << 22) + 5
+
+
+@pytest.mark.parametrize("with_vals", [False, True])
+@pytest.mark.parametrize("in_place", [False, True])
+def test_skipped_passes_over_many_tiles(with_vals, in_place):
+    keys = u32(41, N_MULTI) & np.uint32(0x00FF00FF)    # passes 1 and 3 skipped
+    vals = synth.iota_u32(N_MULTI) if with_vals else None
+    check("u32", keys, vals, 0, 32, expect_runs=2, algo="reduce_scan", in_place=in_place)
+    got, gv, rec = gpu_sort("u32", keys, vals, 0, 32, algo="reduce_scan", in_place=in_place,
+                            descending=True, want_record=True)
+    ref_k, ref_v = oracle.sort("u32", keys, vals, 0, 32, descending=True)
+    assert np.array_equal(got, ref_k)
+    if with_vals:
+        assert np.array_equal(gv, ref_v)
