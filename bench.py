@@ -243,26 +243,72 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(mhz)}
 
 
+def host_info():
+    """This host's CPU: online cores, the C++ runtime's hardware_concurrency(),
+    and the model from /proc/cpuinfo (x86 "model name"; on Arm the
+    implementer and part codes)."""
+    import oracle
+    model, impl, part = None, None, None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                k, v = k.strip().lower(), v.strip()
+                if k in ("model name", "hardware") and v and model is None:
+                    model = v
+                elif k == "cpu implementer" and impl is None:
+                    impl = v
+                elif k == "cpu part" and part is None:
+                    part = v
+    except OSError:
+        pass
+    if model is None and impl is not None:
+        model = f"arm implementer {impl} part {part}"
+    return {"cores_online": os.cpu_count(), "hardware_concurrency": oracle.hardware_concurrency(),
+            "cpu_model": model}
+
+
+def _timed(fn, budget_s, max_reps=50):
+    fn()  # warm (pages, caches)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= max_reps:
+            return reps, el
+
+
 def cpu_baseline(workload, key_type, begin_bit, end_bit, log2n, budget_s=10.0):
-    """The CPU oracle (one thread) on a bounded sample of the same workload."""
+    """The CPU oracle (one thread) on a bounded sample of the same workload, and
+    beside it two more single-threaded CPU sorts of smaller samples: one
+    std::stable_sort of the same problem, and the one-bit index-formula sort
+    of "Radix sort を実装 & 測定してみた" (section 測定 times it on the CPU)."""
     import oracle
     import synth
     sample_log2 = min(log2n, 24)
     n = 1 << sample_log2
     keys = workload.keys(n) if log2n is None or workload.log2n == log2n else synth.u32_uniform(n, 1)
     vals = workload.values(n)
-    oracle.sort(key_type, keys[:1024], None if vals is None else vals[:1024], begin_bit, end_bit)
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        oracle.sort(key_type, keys, vals, begin_bit, end_bit)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s or reps >= 50:
-            break
-    return {"value": round(n * reps / el / 1e9, 6), "unit": "Gkeys/s", "cores": 1,
-            "kind": "oracle",
-            "sample": f"{reps} x oracle sort of the first 2^{sample_log2} keys of the workload "
-                      f"({el:.1f} s single-threaded C counting-sort LSD, r=8)"}
+    reps, el = _timed(lambda: oracle.sort(key_type, keys, vals, begin_bit, end_bit), budget_s)
+    out = {"value": round(n * reps / el / 1e9, 6), "unit": "Gkeys/s", "cores": 1,
+           "kind": "oracle",
+           "sample": f"{reps} x oracle sort of the first 2^{sample_log2} keys of the workload "
+                     f"({el:.1f} s single-threaded C counting-sort LSD, r=8)",
+           "host": host_info()}
+    others = []
+    for kind, log2s, fn, what in (
+            ("std::stable_sort", min(sample_log2, 22), oracle.stable_sort_baseline,
+             "single-threaded C++ std::stable_sort of (ordered key bits, index) records"),
+            ("one_bit_split", min(sample_log2, 20), oracle.one_bit_split_sort,
+             "single-threaded one-bit index-formula LSD sort, one pass per key bit")):
+        m = 1 << log2s
+        k, v = keys[:m], None if vals is None else vals[:m]
+        r, t = _timed(lambda: fn(key_type, k, v, begin_bit, end_bit), budget_s / 2)
+        others.append({"kind": kind, "value": round(m * r / t / 1e9, 6), "unit": "Gkeys/s", "cores": 1,
+                       "sample": f"{r} x sort of the first 2^{log2s} keys of the workload ({t:.1f} s, {what})"})
+    out["others"] = others
+    return out
 
 
 # --------------------------------------------------------------- reference
@@ -295,7 +341,8 @@ def run_reference(args):
             "cpu_baseline": {"value": round(value, 6), "unit": "Gkeys/s", "cores": 1,
                              "kind": "oracle",
                              "sample": f"each step sorts the first 2^{sample_log2} keys of the "
-                                       "workload with the single-threaded CPU oracle"},
+                                       "workload with the single-threaded CPU oracle",
+                             "host": host_info()},
             "e2e": {"value": round(value, 6), "unit": "Gkeys/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

@@ -24,6 +24,11 @@ Functions:
       int32).
   exclusive_scan(values)
       the exclusive prefix sum ("高性能计算：GPU上的基数排序", section CPU上的扫描).
+  stable_sort_baseline(key_type, keys, values=None, begin_bit=0, end_bit=None, descending=False)
+      the same problem as one std::stable_sort (stable_sort_baseline.cpp): a CPU
+      baseline for the bench and a cross-check for the tests.
+  hardware_concurrency()
+      std::thread::hardware_concurrency() of this host.
 """
 from __future__ import annotations
 
@@ -36,6 +41,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
+_SRC_CPP = os.path.join(_HERE, "stable_sort_baseline.cpp")
 _LIBDIR = os.path.join(_HERE, "_lib")
 _LIB = os.path.join(_LIBDIR, "liboracle.so")
 _lock = threading.Lock()
@@ -48,13 +54,22 @@ KEY_BITS = {"u32": 32, "i32": 32, "f32": 32, "u64": 64, "u16": 16, "i16": 16, "f
 
 
 def build(force: bool = False) -> str:
-    """Compile oracle.c into a shared library (host C compiler, -O2, no vectorisation flags)."""
+    """Compile oracle.c (host C compiler) and stable_sort_baseline.cpp (host C++
+    compiler) into one shared library, -O2, no vectorisation flags."""
     with _lock:
-        if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        newest = max(os.path.getmtime(_SRC), os.path.getmtime(_SRC_CPP))
+        if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
             os.makedirs(_LIBDIR, exist_ok=True)
-            tmp = _LIB + f".{os.getpid()}.tmp"
-            subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC])
+            tag = f".{os.getpid()}"
+            obj_c = os.path.join(_LIBDIR, "oracle.o" + tag)
+            obj_cpp = os.path.join(_LIBDIR, "stable_sort_baseline.o" + tag)
+            tmp = _LIB + tag + ".tmp"
+            subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-c", "-o", obj_c, _SRC])
+            subprocess.check_call(["g++", "-O2", "-std=c++17", "-fPIC", "-c", "-o", obj_cpp, _SRC_CPP])
+            subprocess.check_call(["g++", "-shared", "-o", tmp, obj_c, obj_cpp])
             os.replace(tmp, _LIB)
+            os.remove(obj_c)
+            os.remove(obj_cpp)
     return _LIB
 
 
@@ -72,6 +87,11 @@ def _bind(lib):
     lib.oracle_ordered_keys.restype = None
     lib.oracle_exclusive_scan.argtypes = [vp, vp, sz]
     lib.oracle_exclusive_scan.restype = None
+    if hasattr(lib, "cpu_stable_sort"):  # absent from the planted-mistake copies of oracle.c
+        lib.cpu_stable_sort.argtypes = [i32, vp, vp, vp, vp, sz, i32, i32, i32]
+        lib.cpu_stable_sort.restype = i32
+        lib.cpu_hardware_concurrency.argtypes = []
+        lib.cpu_hardware_concurrency.restype = ctypes.c_uint
     return lib
 
 
@@ -153,6 +173,29 @@ def exclusive_scan(values, lib=None) -> np.ndarray:
     out = np.empty_like(v)
     (lib or _load()).oracle_exclusive_scan(_vp(v), _vp(out), v.size)
     return out
+
+
+def stable_sort_baseline(key_type: str, keys, values=None, begin_bit: int = 0, end_bit: int | None = None,
+                         descending: bool = False):
+    """The same sort as one single-threaded std::stable_sort; returns (keys_out, values_out or None)."""
+    k = _as_keys(key_type, keys)
+    end_bit = KEY_BITS[key_type] if end_bit is None else end_bit
+    n = k.size
+    ko = np.empty_like(k)
+    vi = None if values is None else np.ascontiguousarray(values, dtype=np.uint32)
+    vo = None if vi is None else np.empty_like(vi)
+    if vi is not None and vi.size != n:
+        raise ValueError("values must match keys in length")
+    rc = _load().cpu_stable_sort(KEY_TYPES[key_type], _vp(k), _vp(ko), _vp(vi), _vp(vo), n, begin_bit, end_bit,
+                                 int(bool(descending)))
+    if rc != 0:
+        raise ValueError(f"cpu_stable_sort failed with code {rc}")
+    return ko, vo
+
+
+def hardware_concurrency() -> int:
+    """std::thread::hardware_concurrency() of this host."""
+    return int(_load().cpu_hardware_concurrency())
 
 
 def load_variant(path: str):

@@ -81,3 +81,15 @@ def test_reference_arm_prints_the_contract_line():
     assert line["config"]["workload"] == "u32_uniform_2p16"
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_cpu_baseline_reports_host_and_extra_sorts():
+    import synth
+    w = synth.WORKLOADS["u32_uniform_2p16"]
+    cb = bench.cpu_baseline(w, w.key_type, w.begin_bit, w.end_bit, w.log2n, budget_s=0.2)
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] > 0
+    host = cb["host"]
+    assert host["cores_online"] >= 1 and host["hardware_concurrency"] >= 1
+    kinds = [o["kind"] for o in cb["others"]]
+    assert kinds == ["std::stable_sort", "one_bit_split"]
+    assert all(o["value"] > 0 and o["cores"] == 1 for o in cb["others"])

@@ -371,6 +371,35 @@ def test_one_bit_path_agrees_with_counting_path():
         assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
+def test_std_stable_sort_agrees_with_the_oracle():
+    # One std::stable_sort of (ordered key bits, index) records solves the same
+    # problem by comparison; it must give the oracle's keys and payload order
+    # for every key type, random bit ranges and both orders (ties in input
+    # order, "Radix sort paralelo sobre el scan", La idea y el requisito de
+    # estabilidad).  Small alphabets force many ties.
+    rng = np.random.default_rng(2024)
+    for kt, bits in [("u32", 32), ("i32", 32), ("f32", 32), ("u64", 64), ("u16", 16), ("i16", 16),
+                     ("f16", 16)]:
+        for trial in range(4):
+            n = int(rng.integers(1, 3000))
+            if kt == "f32":
+                keys = synth.f32_edge(n, 100 + trial)
+            elif bits == 64:
+                keys = synth.u64_uniform(n, 200 + trial)
+            else:
+                raw = synth.u32_uniform(n, 300 + trial)
+                if trial % 2:
+                    raw = raw & np.uint32(0x0F0F000F)  # few distinct values: ties
+                keys = raw.astype(np.uint16) if bits == 16 else raw
+            b = int(rng.integers(0, bits + 1))
+            e = int(rng.integers(b, bits + 1))
+            vals = np.arange(n, dtype=np.uint32)
+            for desc in (False, True):
+                want = oracle.sort(kt, keys, vals, b, e, descending=desc)
+                got = oracle.stable_sort_baseline(kt, keys, vals, b, e, descending=desc)
+                assert np.array_equal(want[0], got[0]) and np.array_equal(want[1], got[1]), (kt, b, e, desc)
+
+
 def test_digit_width_does_not_change_result():
     keys = synth.u32_uniform(5000, 12)
     ref = oracle.sort("u32", keys, np.arange(5000, dtype=np.uint32), 3, 29, radix_bits=8)
