@@ -326,10 +326,15 @@ rs_status rs_sort_host_batches(rs_key_type key_type, int batches, const void* co
  *
  * The first call on a device looks up the array's device address on that
  * device (cudaGetSymbolAddress); make that first call before any stream
- * capture.  Every call shares the one array per device, so calls that overlap
- * on the GPU (on different streams, or from different threads) race; each
- * call clears what must start at zero.  The device error word lives in that
- * array, so rs_device_status cannot be used with this entry point.
+ * capture.  The address is remembered together with the context it belongs
+ * to: after cudaDeviceReset (or with another context current) the next call
+ * looks it up again, so that call too should come before any capture.
+ * Every call shares the one array per device, so calls that overlap on the
+ * GPU (on different streams, or from different threads) race; each call
+ * clears what must start at zero.  The device error word (a look-back wait
+ * that ran out, a failed bounds check) lives in that array and cannot be read
+ * back: callers that need that status sort with rs_sort_keys_u32 and their
+ * own temp, and read it with rs_device_status.
  */
 #define RS_NOALLOC_MAX_N 4194304
 #define RS_NOALLOC_SCRATCH_BYTES 22020096

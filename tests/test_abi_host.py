@@ -207,3 +207,11 @@ def test_package_does_not_import_oracle():
     code = ("import sys; import lsd_radix_sort_key_gb300 as rs; "
             "assert 'oracle' not in sys.modules, 'product imported the oracle'")
     subprocess.check_call([sys.executable, "-c", code], cwd=ROOT)
+
+
+def test_noalloc_limit_matches_the_header():
+    # The binding's NOALLOC_MAX_N is a copy of RS_NOALLOC_MAX_N; the rejection
+    # test on the GPU relies on the two agreeing.
+    text = open(os.path.join(ROOT, "include", "rs.h")).read()
+    m = re.search(r"#define\s+RS_NOALLOC_MAX_N\s+(\d+)", text)
+    assert m and int(m.group(1)) == rs.NOALLOC_MAX_N

@@ -1,14 +1,16 @@
 """The allocation-free entry point (rs_sort_keys_u32_noalloc), for callers
 that cannot allocate device memory where they sort.
 
-It is checked against the ordinary entry point (rs_sort_keys_u32, with a
-caller-provided temp) on two calls in a row, bit for bit -- the tolerance
-every other sort test uses.  This file is collected last on purpose.
+Its output is checked bit for bit, on two calls in a row, against the CPU
+oracle and against the ordinary entry point (rs_sort_keys_u32, with a
+caller-provided temp) -- the tolerance every other sort test uses.  This file
+is collected last on purpose.
 """
 import numpy as np
 import pytest
 
 import lsd_radix_sort_key_gb300 as rs
+import oracle
 import synth
 
 pytestmark = pytest.mark.gpu
@@ -39,6 +41,8 @@ def test_noalloc_matches_the_temp_buffer_entry_point():
         outs.append((kin, kout, n, b, e))
     torch.cuda.synchronize()
     for kin, kout, n, b, e in outs:
+        want, _ = oracle.sort("u32", kin.cpu().numpy().view(np.uint32), None, b, e)
+        assert np.array_equal(kout.cpu().numpy().view(np.uint32), want)
         ref = reference_sort(kin, n, b, e)
         torch.cuda.synchronize()
         assert torch.equal(kout, ref)
