@@ -842,8 +842,12 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
 // position is sbase[d] + s (sbase = global offset of the digit's run minus
 // its tile-local start).  Consecutive slots mostly share a digit, so each
 // warp store covers few, contiguous segments.  Positions are bounds-checked
-// (a failure is recorded and the store skipped).
-template <bool FULL, int KT, int RB, int THREADS, int ITEMS, int VB>
+// (a failure is recorded and the store skipped).  KEEP marks the stored lines
+// evict-last in L2: in reduce-then-scan the next tile of the same CTA soon
+// fills the rest of each digit run's last, half-written line; the chained
+// scan's neighbouring tiles run on other CTAs at other times, and there the
+// hint measured slower (2^28 uint32 keys: 1.10 vs 1.14 ms per pass).
+template <bool FULL, int KT, int RB, int THREADS, int ITEMS, int VB, bool KEEP = true>
 __device__ __forceinline__ void tile_scatter(const PassParams& p, unsigned char* smem, uint32_t tile,
                                              typename KeyOps<KT>::T* out, ValT<VB>* vout)
 {
@@ -856,7 +860,7 @@ __device__ __forceinline__ void tile_scatter(const PassParams& p, unsigned char*
     const uint32_t tile_base = tile * (uint32_t)TILE;
     const uint32_t valid = FULL ? (uint32_t)TILE : p.n - tile_base;
     uint32_t bad = 0;
-    const uint64_t pol = l2_evict_last_policy();  // half-written lines stay until the next tile fills them
+    const uint64_t pol = KEEP ? l2_evict_last_policy() : 0ull;
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
         const uint32_t s = (uint32_t)(k * THREADS) + threadIdx.x;
@@ -866,8 +870,13 @@ __device__ __forceinline__ void tile_scatter(const PassParams& p, unsigned char*
             const bool ok = idx < p.n;
             bad |= !ok;
             if (ok) {
-                st_keep(out + idx, kk, pol);
-                if constexpr (VB != 0) st_keep(vout + idx, svals[s], pol);
+                if constexpr (KEEP) {
+                    st_keep(out + idx, kk, pol);
+                    if constexpr (VB != 0) st_keep(vout + idx, svals[s], pol);
+                } else {
+                    out[idx] = kk;
+                    if constexpr (VB != 0) vout[idx] = svals[s];
+                }
             }
         }
     }
@@ -988,7 +997,7 @@ __device__ __forceinline__ void onesweep_tile(const PassParams& p, unsigned char
     T* out = io_keys_out<S, T>(smem);
     ValT<VB>* vout = VB ? io_vals_out<S, ValT<VB>>(smem) : nullptr;
     __syncthreads();
-    tile_scatter<FULL, KT, RB, THREADS, ITEMS, VB>(p, smem, tile, out, vout);
+    tile_scatter<FULL, KT, RB, THREADS, ITEMS, VB, false>(p, smem, tile, out, vout);
 }
 
 // Chained-scan pass: one tile per CTA, in the order of an atomic ticket, so
