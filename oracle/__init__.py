@@ -29,6 +29,9 @@ Functions:
       baseline for the bench and a cross-check for the tests.
   hardware_concurrency()
       std::thread::hardware_concurrency() of this host.
+  lbvh_build(sorted_codes)
+      the binary radix tree (linear BVH hierarchy) over sorted codes, built
+      top-down from its definition (lbvh.c).
 """
 from __future__ import annotations
 
@@ -42,6 +45,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _SRC_CPP = os.path.join(_HERE, "stable_sort_baseline.cpp")
+_SRC_LBVH = os.path.join(_HERE, "lbvh.c")
 _LIBDIR = os.path.join(_HERE, "_lib")
 _LIB = os.path.join(_LIBDIR, "liboracle.so")
 _lock = threading.Lock()
@@ -57,19 +61,21 @@ def build(force: bool = False) -> str:
     """Compile oracle.c (host C compiler) and stable_sort_baseline.cpp (host C++
     compiler) into one shared library, -O2, no vectorisation flags."""
     with _lock:
-        newest = max(os.path.getmtime(_SRC), os.path.getmtime(_SRC_CPP))
+        newest = max(os.path.getmtime(_SRC), os.path.getmtime(_SRC_CPP), os.path.getmtime(_SRC_LBVH))
         if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
             os.makedirs(_LIBDIR, exist_ok=True)
             tag = f".{os.getpid()}"
             obj_c = os.path.join(_LIBDIR, "oracle.o" + tag)
             obj_cpp = os.path.join(_LIBDIR, "stable_sort_baseline.o" + tag)
+            obj_lbvh = os.path.join(_LIBDIR, "lbvh.o" + tag)
             tmp = _LIB + tag + ".tmp"
             subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-c", "-o", obj_c, _SRC])
+            subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-c", "-o", obj_lbvh, _SRC_LBVH])
             subprocess.check_call(["g++", "-O2", "-std=c++17", "-fPIC", "-c", "-o", obj_cpp, _SRC_CPP])
-            subprocess.check_call(["g++", "-shared", "-o", tmp, obj_c, obj_cpp])
+            subprocess.check_call(["g++", "-shared", "-o", tmp, obj_c, obj_lbvh, obj_cpp])
             os.replace(tmp, _LIB)
-            os.remove(obj_c)
-            os.remove(obj_cpp)
+            for o in (obj_c, obj_lbvh, obj_cpp):
+                os.remove(o)
     return _LIB
 
 
@@ -92,6 +98,8 @@ def _bind(lib):
         lib.cpu_stable_sort.restype = i32
         lib.cpu_hardware_concurrency.argtypes = []
         lib.cpu_hardware_concurrency.restype = ctypes.c_uint
+        lib.oracle_lbvh_build.argtypes = [vp, sz, vp, vp, vp, vp, vp, vp]
+        lib.oracle_lbvh_build.restype = i32
     return lib
 
 
@@ -196,6 +204,26 @@ def stable_sort_baseline(key_type: str, keys, values=None, begin_bit: int = 0, e
 def hardware_concurrency() -> int:
     """std::thread::hardware_concurrency() of this host."""
     return int(_load().cpu_hardware_concurrency())
+
+
+LBVH_LEAF = 0x80000000
+LBVH_NONE = 0xFFFFFFFF
+
+
+def lbvh_build(sorted_codes) -> dict:
+    """The binary radix tree over sorted uint32 codes: a dict of uint32 arrays
+    left, right, first, last, node_parent (n-1 each) and leaf_parent (n);
+    a child with bit 31 set (LBVH_LEAF) is a leaf."""
+    c = np.ascontiguousarray(sorted_codes, dtype=np.uint32)
+    n = c.size
+    m = max(n - 1, 0)
+    out = {k: np.empty(m, dtype=np.uint32) for k in ("left", "right", "first", "last", "node_parent")}
+    out["leaf_parent"] = np.empty(n, dtype=np.uint32)
+    rc = _load().oracle_lbvh_build(_vp(c), n, *(_vp(out[k]) for k in
+                                                ("left", "right", "first", "last", "leaf_parent", "node_parent")))
+    if rc != 0:
+        raise ValueError(f"oracle_lbvh_build failed with code {rc}")
+    return out
 
 
 def load_variant(path: str):
