@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--radix-bits", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--lbvh", action="store_true",
+                    help="time the LBVH radix-tree build over the sorted codes of the workload "
+                         "(default workload then morton30_index_2p28) instead of the sort")
     return ap.parse_args()
 
 
@@ -348,6 +351,74 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------- lbvh
+
+def run_lbvh(args):
+    """Time rs_lbvh_build over the workload's codes, sorted once on the device
+    by the library beforehand (outside the timed region).  One line of JSON:
+    Gnodes/s (internal nodes built per second) and the kernel against HBM:
+    its algorithmic bytes are the codes read once (4 B each) plus the six
+    output arrays written once (5 x 4 B per internal node, 4 B per leaf)."""
+    import numpy as np
+    import torch
+
+    import lsd_radix_sort_key_gb300 as rs
+    import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    rs.lib()
+    name = args.workload if args.workload != DEFAULT_WORKLOAD else "morton30_index_2p28"
+    w = synth.WORKLOADS[name]
+    if w.key_type != "u32":
+        raise SystemExit("--lbvh needs a workload of uint32 codes")
+    n = w.n
+    host = torch.empty(n, dtype=torch.int32).pin_memory()
+    w.keys(out=host.numpy().view(np.uint32))
+    kin = host.to(dev)
+    vin = torch.arange(n, dtype=torch.int32, device=dev)
+    codes, _ = rs.sort(kin, vin, key_type="u32", begin_bit=w.begin_bit, end_bit=w.end_bit)
+    del kin, vin
+    out = {k: torch.empty(n - 1, dtype=torch.int32, device=dev)
+           for k in ("left", "right", "first", "last", "node_parent")}
+    out["leaf_parent"] = torch.empty(n, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def build():
+        st = rs.rs_lbvh_build(codes, n, out["left"], out["right"], out["first"], out["last"],
+                              out["leaf_parent"], out["node_parent"], stream)
+        assert st == 0, rs.STATUS.get(st)
+
+    for _ in range(max(args.warmup, 3)):
+        build()
+    torch.cuda.synchronize(dev)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    clocks = ClockSampler(0)
+    clocks.start()
+    evs[0].record(stream)
+    for s in range(args.steps):
+        build()
+        evs[s + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    per = [evs[s].elapsed_time(evs[s + 1]) for s in range(args.steps)]
+    ms = statistics.mean(per)
+    peaks, peak_kind = measured_peaks()
+    alg = 4 * n + 20 * (n - 1) + 4 * n
+    achieved = alg / (ms * 1e-3) / 1e9
+    line = {"metric": f"Gnodes/s (LBVH radix tree over {n} sorted Morton codes) on 1 GB300",
+            "value": round((n - 1) / (ms * 1e-3) / 1e9, 3), "unit": "Gnodes/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+            "data": "synthetic", "config": {"workload": name, "n": n, "inputs": "larger than L2, no flush",
+                                             "codes": "sorted by rs_sort_pairs_u32 before the timed region"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                         "algorithmic_bytes_per_launch": alg},
+            "gpu_launches": args.steps, "clocks": clk}
+    print(json.dumps(line), flush=True)
+
+
 # --------------------------------------------------------------------- ours
 
 def run_ours(args):
@@ -603,6 +674,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.lbvh:
+        run_lbvh(args)
     else:
         run_ours(args)
 

@@ -310,6 +310,44 @@ rs_status rs_sort_host_batches(rs_key_type key_type, int batches, const void* co
                                void* d_work, size_t work_bytes, void* stream);
 
 /*
+ * The binary radix tree over sorted Morton codes: the hierarchy of a linear
+ * BVH, the consumer that "高性能计算：GPU上的基数排序" (opening sections)
+ * names as the reason to sort on the GPU.  The page stops at the sort; the
+ * tree follows the published per-node construction of Karras (2012).
+ *
+ * sorted_codes: n uint32 codes in ascending order on the device (for example
+ * the keys_out of rs_sort_pairs_u32 over Morton codes, whose values_out then
+ * maps leaf i back to its primitive).  Equal codes are allowed: leaves are
+ * ordered by (code, position), i.e. the tree is the radix tree of the
+ * distinct 64-bit keys (code << 32) | position.
+ * Outputs (caller-owned device arrays, written in full):
+ *   left[n-1], right[n-1]  children of internal node i: an internal node's
+ *                          index, or a leaf's index with bit 31 set
+ *                          (RS_LBVH_LEAF);
+ *   first[n-1], last[n-1]  the leaf range [first, last] internal node i
+ *                          covers; one end is always i, and node 0 (the root)
+ *                          covers [0, n-1];
+ *   leaf_parent[n]         the internal node above each leaf
+ *                          (0xFFFFFFFF when n == 1);
+ *   node_parent[n-1]       the internal node above each internal node
+ *                          (0xFFFFFFFF for the root).
+ * A node covering [first, last] splits after the last leaf whose key has a 0
+ * in the highest bit where the keys of leaves first and last differ; its left
+ * child covers [first, split] (internal node `split` unless that is one
+ * leaf), its right child [split + 1, last] (internal node `split + 1` unless
+ * one leaf).  One kernel of n - 1 threads, asynchronous on `stream`; no
+ * allocation.  Unsorted codes give an unspecified tree, still written within
+ * the arrays' bounds.  n == 0: RS_OK, nothing enqueued; n == 1: only
+ * leaf_parent[0] is written (the other pointers may be NULL).  Errors:
+ * RS_ERR_INVALID_ARG (n > RS_LBVH_MAX_N, a NULL pointer), RS_ERR_CUDA.
+ */
+#define RS_LBVH_LEAF 0x80000000u
+#define RS_LBVH_MAX_N 2147483648u
+rs_status rs_lbvh_build(const uint32_t* sorted_codes, size_t n, uint32_t* left, uint32_t* right,
+                        uint32_t* first, uint32_t* last, uint32_t* leaf_parent, uint32_t* node_parent,
+                        void* stream);
+
+/*
  * Sort without any allocation.  The pages have no counterpart to this entry
  * point; it exists for callers that cannot allocate device memory where they
  * sort: code running while a stream capture in global mode is active (where

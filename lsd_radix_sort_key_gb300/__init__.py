@@ -72,6 +72,8 @@ SIGNATURES = {
     "rs_sort_host_batches": (_i, [_i, _i, _vp, _vp, _vp, _vp, _sz, _i, _i, _vp, _sz, _vp]),
 }
 SIGNATURES["rs_sort_keys_u32_noalloc"] = (_i, [_vp, _vp, _sz, _i, _i, _vp])
+SIGNATURES["rs_lbvh_build"] = (_i, [_vp, _sz, _vp, _vp, _vp, _vp, _vp, _vp, _vp])
+LBVH_LEAF = 0x80000000
 NOALLOC_MAX_N = 1 << 22
 MAX_N = (1 << 32) - (1 << 16)  # RS_MAX_N
 for _t in ("u32", "i32", "f32", "u64", "u16", "i16", "f16"):
@@ -172,6 +174,31 @@ def rs_sort_keys_u32_noalloc(keys_in, keys_out, n, begin_bit, end_bit, stream=No
     library (no allocation anywhere; n <= NOALLOC_MAX_N)."""
     return lib().rs_sort_keys_u32_noalloc(_addr(keys_in), _addr(keys_out), n, begin_bit, end_bit,
                                           _stream(stream))
+
+
+def rs_lbvh_build(sorted_codes, n, left, right, first, last, leaf_parent, node_parent, stream=None) -> int:
+    """The binary radix tree over n sorted uint32 codes (see include/rs.h)."""
+    return lib().rs_lbvh_build(_addr(sorted_codes), n, _addr(left), _addr(right), _addr(first), _addr(last),
+                               _addr(leaf_parent), _addr(node_parent), _stream(stream))
+
+
+def lbvh_build(sorted_codes, stream=None) -> dict:
+    """rs_lbvh_build with its outputs allocated by torch on the codes' device:
+    a dict of int32 tensors (uint32 bit patterns) left, right, first, last,
+    node_parent (n-1 each) and leaf_parent (n).  Enqueued on `stream`, not
+    synchronised."""
+    import torch
+    if sorted_codes.element_size() != 4 or not sorted_codes.is_contiguous() or not sorted_codes.is_cuda:
+        raise ValueError("codes must be a contiguous CUDA tensor of 4-byte elements")
+    n = sorted_codes.numel()
+    m = max(n - 1, 0)
+    dev = sorted_codes.device
+    out = {k: torch.empty(m, dtype=torch.int32, device=dev)
+           for k in ("left", "right", "first", "last", "node_parent")}
+    out["leaf_parent"] = torch.empty(n, dtype=torch.int32, device=dev)
+    _check(rs_lbvh_build(sorted_codes, n, out["left"], out["right"], out["first"], out["last"],
+                         out["leaf_parent"], out["node_parent"], stream), "rs_lbvh_build")
+    return out
 
 
 def make_desc(key_type, keys_in, keys_out, vals_in, vals_out, n, begin_bit, end_bit, temp,
