@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--radix-bits", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--lib", default=None,
+                    help="path of a variant build of librs.so (python -m lsd_radix_sort_key_gb300._build "
+                         "--libdir DIR --flags ...) to run instead of the default one")
     ap.add_argument("--lbvh", action="store_true",
                     help="time the LBVH radix-tree build over the sorted codes of the workload "
                          "(default workload then morton30_index_2p28) instead of the sort")
@@ -370,6 +373,10 @@ def run_lbvh(args):
     rs.lib()
     name = args.workload if args.workload != DEFAULT_WORKLOAD else "morton30_index_2p28"
     w = synth.WORKLOADS[name]
+    if args.log2n is not None:  # the same codes at another size (a prefix of the same stream)
+        import dataclasses
+        w = dataclasses.replace(w, log2n=args.log2n)
+        name = f"{name}@2p{args.log2n}"
     if w.key_type != "u32":
         raise SystemExit("--lbvh needs a workload of uint32 codes")
     n = w.n
@@ -672,6 +679,9 @@ def run_ours(args):
 
 def main():
     args = parse()
+    if args.lib:
+        import lsd_radix_sort_key_gb300 as rs
+        rs.LIB_PATH = os.path.abspath(args.lib)
     if args.impl == "reference":
         run_reference(args)
     elif args.lbvh:

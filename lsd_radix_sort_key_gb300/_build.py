@@ -79,4 +79,13 @@ def build(force: bool = False, extra_flags=(), verbose: bool = False, libdir: st
 
 
 if __name__ == "__main__":
-    print(build(force=True, verbose=True))
+    # python -m lsd_radix_sort_key_gb300._build [--libdir DIR --flags "-DNAME=VALUE ..."]
+    # builds the library, or a variant of it (compile-time switches, e.g. the
+    # shapes in rs_config.h) into DIR, and prints the library's path.
+    import argparse
+    import shlex
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--libdir", default=None)
+    ap.add_argument("--flags", default="")
+    a = ap.parse_args()
+    print(build(force=True, verbose=True, extra_flags=shlex.split(a.flags), libdir=a.libdir))
