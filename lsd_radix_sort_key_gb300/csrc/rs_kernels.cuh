@@ -1632,7 +1632,11 @@ struct HistParams {
 // COLS, so the COLS lanes of a warp that share no column hit distinct banks:
 // the shared atomics of one warp instruction do not conflict (the warps of
 // the CTA still share the columns, which the atomics make safe).
-template <int KT, int RB, int THREADS, int COLS, bool FULLRANGE>
+// BYTES: every pass's digit is one whole byte of the ordered key (8-bit
+// digits over the full key, ascending), so all MAXP passes run, each digit is
+// one byte permute and each counter address a constant offset from the
+// byte's: the kernel is issue-bound, and this halves its instructions.
+template <int KT, int RB, int THREADS, int COLS, bool FULLRANGE, bool BYTES = false>
 __global__ void __launch_bounds__(THREADS) k_histogram(HistParams h)
 {
     using T = typename KeyOps<KT>::T;
@@ -1660,13 +1664,24 @@ __global__ void __launch_bounds__(THREADS) k_histogram(HistParams h)
         mk[q] = (1u << width) - 1u;
         fl[q] = h.descending ? mk[q] : 0u;
     }
+    static_assert(!BYTES || (RB == 8 && FULLRANGE), "byte digits need 8-bit digits over the whole key");
+    uint32_t* const hcol = hist + col;
     auto count = [&](T k) {
         const auto o = KeyOps<KT>::ordered(k);
+        if constexpr (BYTES) {
 #pragma unroll
-        for (int q = 0; q < MAXP; ++q) {
-            if ((uint32_t)q < h.passes) {
-                const uint32_t d = ((uint32_t)(o >> sh[q]) & mk[q]) ^ fl[q];
-                atomicAdd(hist + (q * BINS + d) * COLS + col, 1u);
+            for (int q = 0; q < MAXP; ++q) {
+                const uint32_t word = (uint32_t)((uint64_t)o >> (32 * (q / 4)));
+                const uint32_t d = __byte_perm(word, 0u, 0x4440u | (uint32_t)(q & 3));
+                atomicAdd(hcol + (q * BINS) * COLS + d * COLS, 1u);
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < MAXP; ++q) {
+                if ((uint32_t)q < h.passes) {
+                    const uint32_t d = ((uint32_t)(o >> sh[q]) & mk[q]) ^ fl[q];
+                    atomicAdd(hist + (q * BINS + d) * COLS + col, 1u);
+                }
             }
         }
     };
@@ -1904,7 +1919,9 @@ rs_status run_passes(Plan& pl)
         constexpr int MAXP = (8 * KB + RB - 1) / RB;
         constexpr int HCOLS = (MAXP * (1 << RB) * 32 * 4 <= 160 * 1024) ? 32 : 16;
         const bool full_range = pl.begin_bit == 0 && pl.end_bit == 8 * KB;
-        auto hk = full_range ? k_histogram<KT, RB, 1024, HCOLS, true> : k_histogram<KT, RB, 1024, HCOLS, false>;
+        auto hk = !full_range                    ? k_histogram<KT, RB, 1024, HCOLS, false>
+                  : (RB == 8 && !pl.descending) ? k_histogram<KT, RB, 1024, HCOLS, true, RB == 8>
+                                                : k_histogram<KT, RB, 1024, HCOLS, true>;
         auto pk = k_onesweep<KT, RB, THREADS, ITEMS, VB>;
         auto pkb = k_onesweep<ByteTwin<KT>::value, RB, THREADS, ITEMS, VB>;
         if (!pl.count_only && (!set_smem(pk, S::bytes) || !set_smem(pkb, S::bytes))) return RS_ERR_CUDA;

@@ -31,12 +31,14 @@ namespace {
 constexpr uint32_t kLeafFlag = 0x80000000u;
 constexpr uint32_t kNone = 0xFFFFFFFFu;
 
-// Common prefix length of key(i) and key(j); -1 if j is outside [0, n).
-__device__ __forceinline__ int delta(const uint32_t* __restrict__ codes, uint32_t n, int64_t i, int64_t j)
+// Common prefix length of key(i) and key(j), given code ci = codes[i]; -1
+// if j is outside [0, n).
+__device__ __forceinline__ int delta(const uint32_t* __restrict__ codes, uint32_t n, int64_t i, uint32_t ci,
+                                     int64_t j)
 {
     if (j < 0 || j >= (int64_t)n) return -1;
-    const uint32_t a = __ldg(codes + i), b = __ldg(codes + j);
-    if (a != b) return __clz(a ^ b);
+    const uint32_t b = __ldg(codes + j);
+    if (ci != b) return __clz(ci ^ b);
     return 32 + __clz((uint32_t)i ^ (uint32_t)j);
 }
 
@@ -49,24 +51,25 @@ __global__ void __launch_bounds__(256) k_lbvh_build(const uint32_t* __restrict__
     const uint32_t nodes = n - 1;
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < nodes; i += gridDim.x * blockDim.x) {
         const int64_t ii = i;
+        const uint32_t ci = __ldg(codes + i);
         // Direction of the range: towards the neighbour sharing the longer prefix.
-        const int d = (delta(codes, n, ii, ii + 1) - delta(codes, n, ii, ii - 1)) >= 0 ? 1 : -1;
+        const int d = (delta(codes, n, ii, ci, ii + 1) - delta(codes, n, ii, ci, ii - 1)) >= 0 ? 1 : -1;
         // The far end: every key in the range shares more than delta_min with key(i).
-        const int delta_min = delta(codes, n, ii, ii - d);
+        const int delta_min = delta(codes, n, ii, ci, ii - d);
         int64_t lmax = 2;
-        while (delta(codes, n, ii, ii + lmax * d) > delta_min) lmax *= 2;
+        while (delta(codes, n, ii, ci, ii + lmax * d) > delta_min) lmax *= 2;
         int64_t l = 0;
         for (int64_t t = lmax / 2; t >= 1; t /= 2)
-            if (delta(codes, n, ii, ii + (l + t) * d) > delta_min) l += t;
+            if (delta(codes, n, ii, ci, ii + (l + t) * d) > delta_min) l += t;
         const int64_t j = ii + l * d;
         // The split: the last key (from i towards j) sharing more than the
         // node's own prefix with key(i).
-        const int delta_node = delta(codes, n, ii, j);
+        const int delta_node = delta(codes, n, ii, ci, j);
         int64_t s = 0;
         int64_t t = l;
         do {
             t = (t + 1) / 2;
-            if (delta(codes, n, ii, ii + (s + t) * d) > delta_node) s += t;
+            if (delta(codes, n, ii, ci, ii + (s + t) * d) > delta_node) s += t;
         } while (t > 1);
         const int64_t gamma = ii + s * d + (d < 0 ? -1 : 0);
         const int64_t lo = ii < j ? ii : j, hi = ii < j ? j : ii;
