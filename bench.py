@@ -651,6 +651,11 @@ def run_ours(args):
                     [outs_v[i % 2] for i in range(k)] if host_v is not None else None)
         assert rs.rs_sort_host_batches(kt, *batches(2), n, b, e, work2, wb2, stream) == 0
         torch.cuda.synchronize(dev)
+        # The host link is sampled right before and right after the timed
+        # region: its speed varies over time on a shared host (1 GiB copies
+        # measured from 5 ms to 37 ms on one box), and the pipelined step
+        # cannot beat the both-directions time of that moment.
+        link_before = link_times(host_k, outs_k[0], work2, dev)
         barrier(pg)
         s0.record(stream)
         assert rs.rs_sort_host_batches(kt, *batches(e2e_steps), n, b, e, work2, wb2, stream) == 0
@@ -666,7 +671,8 @@ def run_ours(args):
                        "d2h_bytes_per_step": n * (kbytes + vbytes),
                        "ms_per_step": round(pipe_ms, 3), "steps": e2e_steps,
                        "api": "rs_sort_host_batches (pinned host buffers, one batch per step, pipelined)",
-                       "serial": serial, "link": link_times(host_k, outs_k[0], work2, dev)}
+                       "serial": serial, "link_before": link_before,
+                       "link": link_times(host_k, outs_k[0], work2, dev)}
         del work2
 
     if rank == 0 and not args.no_cpu:
