@@ -287,9 +287,10 @@ def _timed(fn, budget_s, max_reps=50):
 
 def cpu_baseline(workload, key_type, begin_bit, end_bit, log2n, budget_s=10.0):
     """The CPU oracle (one thread) on a bounded sample of the same workload, and
-    beside it two more single-threaded CPU sorts of smaller samples: one
-    std::stable_sort of the same problem, and the one-bit index-formula sort
-    of "Radix sort を実装 & 測定してみた" (section 測定 times it on the CPU)."""
+    beside it three more CPU sorts: one std::stable_sort of the same problem,
+    the one-bit index-formula sort of "Radix sort を実装 & 測定してみた"
+    (section 測定 times it on the CPU), both single-threaded on smaller
+    samples, and a multi-threaded LSD radix sort on all host threads."""
     import oracle
     import synth
     sample_log2 = min(log2n, 24)
@@ -303,15 +304,19 @@ def cpu_baseline(workload, key_type, begin_bit, end_bit, log2n, budget_s=10.0):
                      f"({el:.1f} s single-threaded C counting-sort LSD, r=8)",
            "host": host_info()}
     others = []
-    for kind, log2s, fn, what in (
+    par_threads = oracle.parallel_threads()
+    for kind, log2s, fn, what, cores in (
             ("std::stable_sort", min(sample_log2, 22), oracle.stable_sort_baseline,
-             "single-threaded C++ std::stable_sort of (ordered key bits, index) records"),
+             "single-threaded C++ std::stable_sort of (ordered key bits, index) records", 1),
             ("one_bit_split", min(sample_log2, 20), oracle.one_bit_split_sort,
-             "single-threaded one-bit index-formula LSD sort, one pass per key bit")):
+             "single-threaded one-bit index-formula LSD sort, one pass per key bit", 1),
+            ("parallel_lsd", sample_log2, oracle.parallel_lsd_sort,
+             f"multi-threaded 8-bit LSD radix sort, one block per thread, on {par_threads} host threads",
+             par_threads)):
         m = 1 << log2s
         k, v = keys[:m], None if vals is None else vals[:m]
         r, t = _timed(lambda: fn(key_type, k, v, begin_bit, end_bit), budget_s / 2)
-        others.append({"kind": kind, "value": round(m * r / t / 1e9, 6), "unit": "Gkeys/s", "cores": 1,
+        others.append({"kind": kind, "value": round(m * r / t / 1e9, 6), "unit": "Gkeys/s", "cores": cores,
                        "sample": f"{r} x sort of the first 2^{log2s} keys of the workload ({t:.1f} s, {what})"})
     out["others"] = others
     return out

@@ -32,6 +32,11 @@ Functions:
   lbvh_build(sorted_codes)
       the binary radix tree (linear BVH hierarchy) over sorted codes, built
       top-down from its definition (lbvh.c).
+  parallel_lsd_sort(key_type, keys, values=None, begin_bit=0, end_bit=None, threads=None)
+      a multi-threaded CPU LSD radix sort (parallel_baseline.c, OpenMP when
+      the compiler has it): the all-cores CPU baseline of the bench.
+  parallel_threads()
+      how many threads that sort uses by default.
 """
 from __future__ import annotations
 
@@ -46,6 +51,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _SRC_CPP = os.path.join(_HERE, "stable_sort_baseline.cpp")
 _SRC_LBVH = os.path.join(_HERE, "lbvh.c")
+_SRC_PAR = os.path.join(_HERE, "parallel_baseline.c")
 _LIBDIR = os.path.join(_HERE, "_lib")
 _LIB = os.path.join(_LIBDIR, "liboracle.so")
 _lock = threading.Lock()
@@ -61,20 +67,34 @@ def build(force: bool = False) -> str:
     """Compile oracle.c (host C compiler) and stable_sort_baseline.cpp (host C++
     compiler) into one shared library, -O2, no vectorisation flags."""
     with _lock:
-        newest = max(os.path.getmtime(_SRC), os.path.getmtime(_SRC_CPP), os.path.getmtime(_SRC_LBVH))
+        newest = max(os.path.getmtime(x) for x in (_SRC, _SRC_CPP, _SRC_LBVH, _SRC_PAR))
         if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
             os.makedirs(_LIBDIR, exist_ok=True)
             tag = f".{os.getpid()}"
             obj_c = os.path.join(_LIBDIR, "oracle.o" + tag)
             obj_cpp = os.path.join(_LIBDIR, "stable_sort_baseline.o" + tag)
             obj_lbvh = os.path.join(_LIBDIR, "lbvh.o" + tag)
+            obj_par = os.path.join(_LIBDIR, "parallel_baseline.o" + tag)
             tmp = _LIB + tag + ".tmp"
             subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-c", "-o", obj_c, _SRC])
             subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-c", "-o", obj_lbvh, _SRC_LBVH])
             subprocess.check_call(["g++", "-O2", "-std=c++17", "-fPIC", "-c", "-o", obj_cpp, _SRC_CPP])
-            subprocess.check_call(["g++", "-shared", "-o", tmp, obj_c, obj_lbvh, obj_cpp])
+            # OpenMP for the multi-threaded baseline when the compiler has it; one thread otherwise
+            omp = ["-fopenmp"]
+            r = subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", *omp, "-c", "-o", obj_par, _SRC_PAR],
+                               capture_output=True)
+            if r.returncode != 0:
+                omp = []
+                subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-c", "-o", obj_par, _SRC_PAR])
+            r = subprocess.run(["g++", "-shared", *omp, "-o", tmp, obj_c, obj_lbvh, obj_par, obj_cpp],
+                               capture_output=True)
+            if r.returncode != 0 and omp:  # no OpenMP runtime to link: build the one-thread form
+                subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-c", "-o", obj_par, _SRC_PAR])
+                subprocess.check_call(["g++", "-shared", "-o", tmp, obj_c, obj_lbvh, obj_par, obj_cpp])
+            elif r.returncode != 0:
+                raise RuntimeError(r.stderr.decode(errors="replace"))
             os.replace(tmp, _LIB)
-            for o in (obj_c, obj_lbvh, obj_cpp):
+            for o in (obj_c, obj_lbvh, obj_par, obj_cpp):
                 os.remove(o)
     return _LIB
 
@@ -100,6 +120,10 @@ def _bind(lib):
         lib.cpu_hardware_concurrency.restype = ctypes.c_uint
         lib.oracle_lbvh_build.argtypes = [vp, sz, vp, vp, vp, vp, vp, vp]
         lib.oracle_lbvh_build.restype = i32
+        lib.cpu_parallel_lsd_sort.argtypes = [i32, vp, vp, vp, vp, sz, i32, i32, i32]
+        lib.cpu_parallel_lsd_sort.restype = i32
+        lib.cpu_parallel_threads.argtypes = []
+        lib.cpu_parallel_threads.restype = i32
     return lib
 
 
@@ -198,6 +222,31 @@ def stable_sort_baseline(key_type: str, keys, values=None, begin_bit: int = 0, e
                                  int(bool(descending)))
     if rc != 0:
         raise ValueError(f"cpu_stable_sort failed with code {rc}")
+    return ko, vo
+
+
+def parallel_threads() -> int:
+    """Threads the multi-threaded baseline uses by default (1 without OpenMP)."""
+    return int(_load().cpu_parallel_threads())
+
+
+def parallel_lsd_sort(key_type: str, keys, values=None, begin_bit: int = 0, end_bit: int | None = None,
+                      threads: int | None = None):
+    """The same sort, ascending, on `threads` host threads (default: all);
+    returns (keys_out, values_out or None)."""
+    k = _as_keys(key_type, keys)
+    end_bit = KEY_BITS[key_type] if end_bit is None else end_bit
+    n = k.size
+    ko = np.empty_like(k)
+    vi = None if values is None else np.ascontiguousarray(values, dtype=np.uint32)
+    vo = None if vi is None else np.empty_like(vi)
+    if vi is not None and vi.size != n:
+        raise ValueError("values must match keys in length")
+    t = parallel_threads() if threads is None else threads
+    rc = _load().cpu_parallel_lsd_sort(KEY_TYPES[key_type], _vp(k), _vp(ko), _vp(vi), _vp(vo), n, begin_bit,
+                                       end_bit, t)
+    if rc != 0:
+        raise ValueError(f"cpu_parallel_lsd_sort failed with code {rc}")
     return ko, vo
 
 

@@ -400,6 +400,29 @@ def test_std_stable_sort_agrees_with_the_oracle():
                 assert np.array_equal(want[0], got[0]) and np.array_equal(want[1], got[1]), (kt, b, e, desc)
 
 
+def test_parallel_baseline_agrees_with_the_oracle():
+    # The multi-threaded CPU baseline (one block per thread, digit-major scan
+    # of the blocks' counts) must give the oracle's keys and payload order on
+    # any number of threads, including more threads than keys.
+    rng = np.random.default_rng(77)
+    for kt, bits in [("u32", 32), ("i32", 32), ("f32", 32), ("u64", 64), ("u16", 16), ("f16", 16)]:
+        n = int(rng.integers(1, 5000))
+        if kt == "f32":
+            keys = synth.f32_edge(n, 400)
+        elif bits == 64:
+            keys = synth.u64_uniform(n, 401)
+        else:
+            raw = synth.u32_uniform(n, 402) & np.uint32(0x0F0F0F0F)
+            keys = raw.astype(np.uint16) if bits == 16 else raw
+        b = int(rng.integers(0, bits))
+        e = int(rng.integers(b, bits + 1))
+        vals = np.arange(n, dtype=np.uint32)
+        want = oracle.sort(kt, keys, vals, b, e)
+        for threads in (1, 2, 7, 64):
+            got = oracle.parallel_lsd_sort(kt, keys, vals, b, e, threads=threads)
+            assert np.array_equal(want[0], got[0]) and np.array_equal(want[1], got[1]), (kt, b, e, threads)
+
+
 def test_digit_width_does_not_change_result():
     keys = synth.u32_uniform(5000, 12)
     ref = oracle.sort("u32", keys, np.arange(5000, dtype=np.uint32), 3, 29, radix_bits=8)
