@@ -372,6 +372,11 @@ template <typename T, int RB, int THREADS, int ITEMS, int VB>
 struct TileSmem {
     static constexpr int BINS = 1 << RB;
     static constexpr int WARPS = THREADS / 32;
+    // Every tile kernel gives each digit its own thread for the per-digit
+    // steps (counts, scans, starts, look-back), and the digit scan runs over
+    // at most 32 warps.
+    static_assert(THREADS >= BINS && THREADS % 32 == 0 && THREADS <= 1024,
+                  "a tile needs at least one thread per digit");
     static constexpr int TILE = THREADS * ITEMS;
     static constexpr int WH = BINS + 1;  // per-array counters + one dummy slot for tail lanes
     static constexpr size_t keys_off = 0;
