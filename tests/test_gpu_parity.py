@@ -138,6 +138,21 @@ def test_float_specials_and_signed_zero():
     assert neg[: int(neg.sum())].all()                 # -0.0 before +0.0
 
 
+@pytest.mark.parametrize("kt", ["u32", "i32", "f32", "u16"])
+@pytest.mark.parametrize("descending", [False, True])
+def test_keys_only_mixed_entropy_chunks(kt, descending):
+    # Keys-only reduce-then-scan over chunks of different digit skew (uniform,
+    # AND of 4, 8 distinct values, one repeated key, uniform), so the CTAs of
+    # one pass see different digit mixes and rank with different match widths.
+    m = 300_001
+    raw = np.concatenate([synth.u32_uniform(m, 41), synth.u32_and4(m, 42), synth.u32_bits(m, 1, 3),
+                          np.full(m, 0x80000001, np.uint32), synth.u32_uniform(m + 777, 43)])
+    keys = (raw >> np.uint32(16)).astype(np.uint16) if kt == "u16" else raw
+    bits = 16 if kt == "u16" else 32
+    got_k, _ = gpu_sort(kt, keys, None, 0, bits, algo="reduce_scan", descending=descending)
+    assert np.array_equal(got_k, oracle.sort(kt, keys, None, 0, bits, descending=descending)[0])
+
+
 def test_many_tiles_onesweep_lookback():
     # > 256 tiles per pass, uneven tail: exercises long look-back chains
     n = (1 << 22) + 12345
