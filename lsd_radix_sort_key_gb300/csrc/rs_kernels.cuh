@@ -379,15 +379,46 @@ struct TileSmem {
                   "a tile needs at least one thread per digit");
     static constexpr int TILE = THREADS * ITEMS;
     static constexpr int WH = BINS + 1;  // per-array counters + one dummy slot for tail lanes
+    // The shuffled tile: slot s holds a key and its value.  A 32-bit key and
+    // a 32-bit value share one 8-byte slot (one shared-memory store and one
+    // load per pair instead of two each); other shapes keep two arrays.
+    static constexpr bool PAIRED = sizeof(T) == 4 && VB == 4;
     static constexpr size_t keys_off = 0;
-    static constexpr size_t vals_off = align_up(sizeof(T) * TILE, 16);
-    static constexpr size_t wh_off = vals_off + (VB ? align_up(sizeof(ValT<VB>) * (size_t)TILE, 16) : 0);
+    static constexpr size_t vals_off = PAIRED ? 0 : align_up(sizeof(T) * TILE, 16);
+    static constexpr size_t wh_off = PAIRED ? align_up(8 * (size_t)TILE, 16)
+                                            : vals_off + (VB ? align_up(sizeof(ValT<VB>) * (size_t)TILE, 16) : 0);
     static constexpr size_t base_off = wh_off + align_up(4 * (size_t)WARPS * WH, 16);
     static constexpr size_t scan_off = base_off + 4 * BINS;
     static constexpr size_t misc_off = scan_off + 4 * 32;
     static constexpr size_t io_off = misc_off + 16;  // this pass's 4 buffer pointers
     static constexpr size_t bytes = io_off + 32;
 };
+
+// Slot s of the shuffled tile (TileSmem::keys_off / vals_off, or the paired
+// slots): store a key and its value, and read them back.
+template <typename S, typename T, int VB>
+__device__ __forceinline__ void slot_put(unsigned char* smem, uint32_t s, T key, ValT<VB> val)
+{
+    if constexpr (S::PAIRED) {
+        reinterpret_cast<uint2*>(smem + S::keys_off)[s] = make_uint2((uint32_t)key, (uint32_t)val);
+    } else {
+        reinterpret_cast<T*>(smem + S::keys_off)[s] = key;
+        if constexpr (VB != 0) reinterpret_cast<ValT<VB>*>(smem + S::vals_off)[s] = val;
+    }
+}
+
+template <typename S, typename T, int VB>
+__device__ __forceinline__ void slot_get(const unsigned char* smem, uint32_t s, T& key, ValT<VB>& val)
+{
+    if constexpr (S::PAIRED) {
+        const uint2 kv = reinterpret_cast<const uint2*>(smem + S::keys_off)[s];
+        key = (T)kv.x;
+        val = kv.y;
+    } else {
+        key = reinterpret_cast<const T*>(smem + S::keys_off)[s];
+        if constexpr (VB != 0) val = reinterpret_cast<const ValT<VB>*>(smem + S::vals_off)[s];
+    }
+}
 
 // ------------------------------------------------------------ pass skipping
 //
@@ -785,8 +816,6 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
     using T = typename KeyOps<KT>::T;
     using S = TileSmem<T, RB, THREADS, ITEMS, VB>;
     constexpr int BINS = S::BINS, TILE = S::TILE, WH = S::WH, WARPS = S::WARPS;
-    T* skeys = reinterpret_cast<T*>(smem + S::keys_off);
-    ValT<VB>* svals = reinterpret_cast<ValT<VB>*>(smem + S::vals_off);
     uint32_t* whist = reinterpret_cast<uint32_t*>(smem + S::wh_off);
     uint32_t* sscan = reinterpret_cast<uint32_t*>(smem + S::scan_off);
 
@@ -834,8 +863,8 @@ __device__ __forceinline__ void tile_rank_and_shuffle(const PassParams& p, unsig
 #endif
         pos = min(pos, (uint32_t)TILE - 1u);
         if (FULL || d < (uint32_t)BINS) {
-            skeys[pos] = key[k];
-            if constexpr (VB != 0) svals[pos] = val[k];
+            if constexpr (VB != 0) slot_put<S, T, VB>(smem, pos, key[k], val[k]);
+            else slot_put<S, T, VB>(smem, pos, key[k], 0u);
         }
     }
     if (bad) record_error(p.err, RS_ERR_CHECK_FAILED);
@@ -859,8 +888,6 @@ __device__ __forceinline__ void tile_scatter(const PassParams& p, unsigned char*
     using T = typename KeyOps<KT>::T;
     using S = TileSmem<T, RB, THREADS, ITEMS, VB>;
     constexpr int TILE = S::TILE;
-    const T* skeys = reinterpret_cast<const T*>(smem + S::keys_off);
-    const ValT<VB>* svals = reinterpret_cast<const ValT<VB>*>(smem + S::vals_off);
     const uint32_t* sbase = reinterpret_cast<const uint32_t*>(smem + S::base_off);
     const uint32_t tile_base = tile * (uint32_t)TILE;
     const uint32_t valid = FULL ? (uint32_t)TILE : p.n - tile_base;
@@ -870,17 +897,19 @@ __device__ __forceinline__ void tile_scatter(const PassParams& p, unsigned char*
     for (int k = 0; k < ITEMS; ++k) {
         const uint32_t s = (uint32_t)(k * THREADS) + threadIdx.x;
         if (FULL || s < valid) {
-            const T kk = skeys[s];
+            T kk;
+            ValT<VB> vv;
+            slot_get<S, T, VB>(smem, s, kk, vv);
             const uint32_t idx = sbase[digit_of<KT>(kk, p.shift, p.mask, p.flip)] + s;
             const bool ok = idx < p.n;
             bad |= !ok;
             if (ok) {
                 if constexpr (KEEP) {
                     st_keep(out + idx, kk, pol);
-                    if constexpr (VB != 0) st_keep(vout + idx, svals[s], pol);
+                    if constexpr (VB != 0) st_keep(vout + idx, vv, pol);
                 } else {
                     out[idx] = kk;
-                    if constexpr (VB != 0) vout[idx] = svals[s];
+                    if constexpr (VB != 0) vout[idx] = vv;
                 }
             }
         }
@@ -1442,8 +1471,6 @@ __global__ void __launch_bounds__(THREADS, 1) k_cluster_sort(ClusterParams cp)
     constexpr int BINS = S::BINS;
     constexpr uint32_t M = S::TILE;
     extern __shared__ __align__(16) unsigned char smem[];
-    const T* skeys = reinterpret_cast<const T*>(smem + S::keys_off);
-    const ValT<VB>* svals = reinterpret_cast<const ValT<VB>*>(smem + S::vals_off);
     uint32_t* sbase = reinterpret_cast<uint32_t*>(smem + S::base_off);
     uint32_t* sscan = reinterpret_cast<uint32_t*>(smem + S::scan_off);
     T* nkeys = reinterpret_cast<T*>(smem + CS::next_keys_off);
@@ -1589,7 +1616,9 @@ __global__ void __launch_bounds__(THREADS, 1) k_cluster_sort(ClusterParams cp)
         for (int k = 0; k < ITEMS; ++k) {
             const uint32_t s = (uint32_t)(k * THREADS) + tid;
             if (s < valid) {
-                const T kk = skeys[s];
+                T kk;
+                ValT<VB> vv;
+                slot_get<S, T, VB>(smem, s, kk, vv);
                 const uint32_t g = sbase[digit_of<KT>(kk, p.shift, p.mask, p.flip)] + s;
                 if (g >= cp.n) {
                     bad = 1;
@@ -1597,11 +1626,11 @@ __global__ void __launch_bounds__(THREADS, 1) k_cluster_sort(ClusterParams cp)
                 }
                 if (last) {
                     gout[g] = kk;
-                    if constexpr (VB != 0) static_cast<ValT<VB>*>(cp.vals_out)[g] = svals[s];
+                    if constexpr (VB != 0) static_cast<ValT<VB>*>(cp.vals_out)[g] = vv;
                 } else {
                     const uint32_t dst = g / M, off = g - dst * M;
                     *cluster.map_shared_rank(nkeys + off, dst) = kk;
-                    if constexpr (VB != 0) *cluster.map_shared_rank(nvals + off, dst) = svals[s];
+                    if constexpr (VB != 0) *cluster.map_shared_rank(nvals + off, dst) = vv;
                 }
             }
         }
