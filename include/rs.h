@@ -103,8 +103,11 @@ typedef enum rs_key_type {
 
 typedef enum rs_algo {
     RS_ALGO_AUTO = 0,        /* the cluster sort for n <= rs_cluster_max_n(),
-                                reduce-then-scan for n >= 2^22, the chained scan
-                                between (measured on GB300)                      */
+                                reduce-then-scan for n >= 2^22 (2^23 for 32-bit
+                                keys with values and for 64-bit keys alone;
+                                never below 2^30 for 64-bit keys with 64-bit
+                                values), the chained scan between (measured
+                                on GB300)                                        */
     RS_ALGO_ONESWEEP = 1,    /* one upfront histogram read + one kernel per pass    */
     RS_ALGO_REDUCE_SCAN = 2, /* upsweep + spine scan + downsweep per pass           */
     RS_ALGO_CLUSTER = 3      /* the whole sort in ONE kernel on a thread-block

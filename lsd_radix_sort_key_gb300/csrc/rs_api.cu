@@ -26,7 +26,20 @@ namespace {
 
 constexpr size_t kMaxN = (size_t)RS_MAX_N;           // 2^32 - 2^16
 constexpr size_t kOnesweepMaxN = ((size_t)1 << 30) - 1;
-constexpr size_t kAutoReduceScanMinN = (size_t)1 << 22;
+// AUTO's smallest reduce-then-scan size for kb-byte keys with vb-byte values
+// (0: none), from graph-replay timings on GB300 (ms per sort, chained scan vs
+// reduce-then-scan): 32-bit keys alone tie at 2^22 (0.105 either way);
+// 32-bit keys with values and 64-bit keys alone lose with reduce-then-scan at
+// 2^22 (u32 + u32: 0.132 vs 0.139; u32 + u64: 0.157 vs 0.161; u64: 0.249 vs
+// 0.287) and win with it from 2^24 (0.419 vs 0.432; 0.541 vs 0.554; 0.800
+// vs 0.828); 64-bit keys with 64-bit values win with the chained scan at every
+// size from 2^24 on (2^28: 21.33 vs 21.86) and tie at 2^22.
+size_t auto_reduce_scan_min_n(int kb, int vb)
+{
+    if (kb == 8 && vb == 8) return kOnesweepMaxN + 1;
+    if ((kb == 8 && vb == 0) || (kb == 4 && vb != 0)) return (size_t)1 << 23;
+    return (size_t)1 << 22;
+}
 constexpr uint32_t kDefaultSpinLimit = 1u << 20;      // each spin is one L2 round trip (~1 s in all)
 
 int key_bytes(rs_key_type kt) { return kt == RS_U64 ? 8 : kt >= RS_U16 ? 2 : 4; }
@@ -82,12 +95,12 @@ rs_status make_plan(const rs_sort_desc* d, rs::Plan* pl)
     const size_t cluster_max = rs::cluster_max_n(kb, vb);
     if (pl->algo == RS_ALGO_AUTO) {
         // Chosen by measurement on GB300: one cluster kernel while the keys fit
-        // in the cluster's shared memory; reduce-then-scan from 2^22 keys (from
-        // there on it beats the chained scan host-launched and graph-replayed,
-        // its 12 kernels' launches hidden by programmatic dependent launch; at
-        // 2^21 the chained scan's 5 kernels still win); the chained scan
-        // between.  The chained scan needs n < 2^30.
-        const bool rts = n > kOnesweepMaxN || n >= kAutoReduceScanMinN;
+        // in the cluster's shared memory; reduce-then-scan from 2^22 or 2^23
+        // keys, by shape (from there on it beats the chained scan
+        // host-launched and graph-replayed, its 12 kernels' launches hidden by
+        // programmatic dependent launch; below, the chained scan's 5 kernels
+        // win); the chained scan between.  The chained scan needs n < 2^30.
+        const bool rts = n > kOnesweepMaxN || n >= auto_reduce_scan_min_n(kb, vb);
         pl->algo = n <= cluster_max ? RS_ALGO_CLUSTER : rts ? RS_ALGO_REDUCE_SCAN : RS_ALGO_ONESWEEP;
         pl->auto_chosen = true;
     }

@@ -51,11 +51,11 @@ def test_temp_bytes_layout(lib):
 
 
 def test_kernel_counts(lib):
-    def count(kt, n, b, e, algo, rb=0, vals=False):
+    def count(kt, n, b, e, algo, rb=0, vals=False, vbytes=0):
         v = 0x3 << 40 if vals else None
         vo = 0x4 << 40 if vals else None
         return rs.rs_sort_kernel_count(rs.make_desc(kt, None, None, v, vo, n, b, e, None, 0, 0,
-                                                    algo, rb))
+                                                    algo, rb, value_bytes=vbytes))
     assert count("u32", 1 << 20, 0, 32, "onesweep") == 1 + 4
     assert count("u32", 1 << 20, 0, 30, "onesweep") == 1 + 4
     assert count("u32", 1 << 20, 0, 32, "onesweep", 4) == 1 + 8
@@ -63,10 +63,23 @@ def test_kernel_counts(lib):
     assert count("u32", 1 << 20, 0, 32, "reduce_scan") == 3 * 4
     assert count("u32", 1 << 20, 7, 7, "onesweep") == 0
     assert count("u32", 0, 0, 32, "onesweep") == 0
-    # AUTO: chained scan below 2^22 keys, reduce-then-scan from there on
+    # AUTO: chained scan below 2^22 keys (2^23 for 32-bit keys with values
+    # and for 64-bit keys alone), reduce-then-scan from there on; 64-bit keys
+    # with 64-bit values always take the chained scan (below its 2^30 limit)
     assert count("u32", 1 << 20, 0, 32, "auto") == 5
+    assert count("u32", (1 << 22) - 1, 0, 32, "auto") == 5
+    assert count("u32", 1 << 22, 0, 32, "auto") == 12
     assert count("u64", (1 << 22) - 1, 0, 64, "auto", vals=True) == 9
     assert count("u64", 1 << 22, 0, 64, "auto", vals=True) == 24
+    assert count("u64", 1 << 22, 0, 64, "auto") == 9
+    assert count("u64", (1 << 23) - 1, 0, 64, "auto") == 9
+    assert count("u64", 1 << 23, 0, 64, "auto") == 24
+    assert count("u32", 1 << 22, 0, 32, "auto", vals=True) == 5
+    assert count("u32", 1 << 23, 0, 32, "auto", vals=True) == 12
+    assert count("u32", 1 << 22, 0, 32, "auto", vals=True, vbytes=8) == 5
+    assert count("u32", 1 << 23, 0, 32, "auto", vals=True, vbytes=8) == 12
+    assert count("u64", 1 << 28, 0, 64, "auto", vals=True, vbytes=8) == 9
+    assert count("u16", 1 << 22, 0, 16, "auto", vals=True) == 6
     assert count("u32", 1 << 26, 0, 32, "auto") == 12
     assert count("u32", 1 << 26, 0, 32, "auto", vals=True) == 12
     assert count("u64", 1 << 26, 0, 64, "auto") == 24
