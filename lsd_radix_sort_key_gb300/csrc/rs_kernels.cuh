@@ -58,6 +58,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <type_traits>
 
 #include "rs.h"
 #include "rs_config.h"
@@ -1944,8 +1945,10 @@ rs_status run_passes(Plan& pl)
         return after_launch(pl, kKindCopy);
     };
 
-    if (pl.algo == RS_ALGO_ONESWEEP) {
-        constexpr int THREADS = tile_threads(kAlgoOnesweep, KB, VB);
+    // The chained scan on tiles of THREADS x ITEMS keys (threads_c carries
+    // THREADS: onesweep_threads() picks it from n).
+    auto run_onesweep = [&](auto threads_c) -> rs_status {
+        constexpr int THREADS = decltype(threads_c)::value;
         constexpr int TILE = THREADS * ITEMS;
         using S = TileSmem<T, RB, THREADS, ITEMS, VB>;
         const uint32_t num_tiles = (n + TILE - 1) / TILE;
@@ -1997,6 +2000,13 @@ rs_status run_passes(Plan& pl)
             if (st != RS_OK) return st;
         }
         return finish();
+    };
+    if (pl.algo == RS_ALGO_ONESWEEP) {
+        if constexpr (RB == 8) {
+            if (onesweep_threads(n, KB, VB, RB) == RS_OS_THREADS_SMALL)
+                return run_onesweep(std::integral_constant<int, RS_OS_THREADS_SMALL>{});
+        }
+        return run_onesweep(std::integral_constant<int, RS_OS_THREADS>{});
     }
 
     // Reduce-then-scan.
