@@ -7,7 +7,8 @@ and through the typed entry points; descending order for every key type,
 including the inputs that skip passes (already in ascending order: nothing
 skipped; already in descending order: every pass skipped), whose skip record
 is checked against its definition; uint64 payloads for 32-, 64- and 16-bit
-keys (expected payloads gathered by the oracle's permutation).
+keys (expected payloads gathered by the oracle's permutation); AUTO's
+schedule for each key/value shape just above 2^22 keys.
 """
 import numpy as np
 import pytest
@@ -170,3 +171,24 @@ def test_64bit_values_unaligned_keys_and_sort_wrapper():
     ref_k, perm = oracle.sort("u32", keys, synth.iota_u32(n), 0, 32, descending=True)
     assert np.array_equal(ko.cpu().numpy().view(np.uint32), ref_k)
     assert np.array_equal(vo.cpu().numpy().view(np.uint64), synth.u64_uniform(n, 1221)[perm])
+
+
+# AUTO picks the schedule by size and shape: 64-bit keys alone and 32-bit
+# keys with values take the chained scan up to 2^23 keys, 64-bit keys with
+# 64-bit values take it at every size it supports.  Each case sorts through
+# AUTO just above 2^22 keys (a ragged last tile) and checks the schedule by
+# its kernel count as well as the result.
+@pytest.mark.parametrize("kt,vb,chained", [("u64", 0, True), ("u32", 4, True), ("u32", 8, True),
+                                           ("u64", 8, True), ("u64", 4, False), ("u32", 0, False)])
+def test_auto_schedule_by_shape(kt, vb, chained):
+    n = (1 << 22) + 5
+    keys = gen_keys(kt, n, 1300 + vb)
+    bits = rs.KEY_BITS[kt]
+    passes = bits // 8
+    vin, vout = ((0x3 << 40), (0x4 << 40)) if vb else (None, None)  # addresses for the count query only
+    d = rs.make_desc(kt, None, None, vin, vout, n, 0, bits, None, 0, 0, "auto", 0, value_bytes=vb)
+    assert rs.rs_sort_kernel_count(d) == (1 + passes if chained else 3 * passes)
+    if vb == 8:
+        check64(kt, keys, 0, bits)
+    else:
+        check(kt, keys, synth.iota_u32(n) if vb else None, 0, bits)
