@@ -31,15 +31,32 @@ namespace {
 constexpr uint32_t kLeafFlag = 0x80000000u;
 constexpr uint32_t kNone = 0xFFFFFFFFu;
 
-// Common prefix length of key(i) and key(j), given code ci = codes[i]; -1
-// if j is outside [0, n).
-__device__ __forceinline__ int delta(const uint32_t* __restrict__ codes, uint32_t n, int64_t i, uint32_t ci,
-                                     int64_t j)
+// Positions are 32-bit: with n <= 2^31, a probe i + l*d (l <= 2^31, the
+// search never doubles past the end of [0, n)) wraps below 0 to a value
+// >= 2^31 >= n, so one unsigned compare rejects both ends.
+__device__ __forceinline__ uint32_t toward(uint32_t i, uint32_t l, int d) { return d > 0 ? i + l : i - l; }
+
+// delta(i, j): the common prefix length of key(i) and key(j), given ci =
+// codes[i]; -1 if j is outside [0, n).
+__device__ __forceinline__ int delta(const uint32_t* __restrict__ codes, uint32_t n, uint32_t i, uint32_t ci,
+                                     uint32_t j)
 {
-    if (j < 0 || j >= (int64_t)n) return -1;
-    const uint32_t b = __ldg(codes + j);
-    if (ci != b) return __clz(ci ^ b);
-    return 32 + __clz((uint32_t)i ^ (uint32_t)j);
+    if (j >= n) return -1;
+    const uint32_t x = ci ^ __ldg(codes + j);
+    return x ? __clz(x) : 32 + __clz(i ^ j);
+}
+
+// delta(i, j) > m, for m in [-1, 63], without counting the prefix: the keys
+// share more than m leading bits exactly when their 64-bit XOR, (code xor)
+// << 32 | (position xor), is below 2^(63 - m).
+__device__ __forceinline__ bool shares_more(const uint32_t* __restrict__ codes, uint32_t n, uint32_t i,
+                                            uint32_t ci, uint32_t j, int m)
+{
+    if (j >= n) return false;
+    const uint32_t hx = ci ^ __ldg(codes + j);
+    const int s = 63 - m;  // 0..64
+    if (s >= 32) return s >= 64 || (hx >> (s - 32)) == 0u;
+    return hx == 0u && ((i ^ j) >> s) == 0u;
 }
 
 __global__ void __launch_bounds__(256) k_lbvh_build(const uint32_t* __restrict__ codes, uint32_t n,
@@ -50,35 +67,32 @@ __global__ void __launch_bounds__(256) k_lbvh_build(const uint32_t* __restrict__
 {
     const uint32_t nodes = n - 1;
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < nodes; i += gridDim.x * blockDim.x) {
-        const int64_t ii = i;
         const uint32_t ci = __ldg(codes + i);
         // Direction of the range: towards the neighbour sharing the longer prefix.
-        const int d = (delta(codes, n, ii, ci, ii + 1) - delta(codes, n, ii, ci, ii - 1)) >= 0 ? 1 : -1;
+        const int d = (delta(codes, n, i, ci, i + 1) - delta(codes, n, i, ci, i - 1)) >= 0 ? 1 : -1;
         // The far end: every key in the range shares more than delta_min with key(i).
-        const int delta_min = delta(codes, n, ii, ci, ii - d);
-        int64_t lmax = 2;
-        while (delta(codes, n, ii, ci, ii + lmax * d) > delta_min) lmax *= 2;
-        int64_t l = 0;
-        for (int64_t t = lmax / 2; t >= 1; t /= 2)
-            if (delta(codes, n, ii, ci, ii + (l + t) * d) > delta_min) l += t;
-        const int64_t j = ii + l * d;
+        const int delta_min = delta(codes, n, i, ci, toward(i, 1, -d));
+        uint32_t lmax = 2;
+        while (shares_more(codes, n, i, ci, toward(i, lmax, d), delta_min)) lmax <<= 1;
+        uint32_t l = 0;
+        for (uint32_t t = lmax >> 1; t >= 1; t >>= 1)
+            if (shares_more(codes, n, i, ci, toward(i, l + t, d), delta_min)) l += t;
+        const uint32_t j = toward(i, l, d);
         // The split: the last key (from i towards j) sharing more than the
         // node's own prefix with key(i).
-        const int delta_node = delta(codes, n, ii, ci, j);
-        int64_t s = 0;
-        int64_t t = l;
+        const int delta_node = delta(codes, n, i, ci, j);
+        uint32_t s = 0, t = l;
         do {
-            t = (t + 1) / 2;
-            if (delta(codes, n, ii, ci, ii + (s + t) * d) > delta_node) s += t;
+            t = (t + 1) >> 1;
+            if (shares_more(codes, n, i, ci, toward(i, s + t, d), delta_node)) s += t;
         } while (t > 1);
-        const int64_t gamma = ii + s * d + (d < 0 ? -1 : 0);
-        const int64_t lo = ii < j ? ii : j, hi = ii < j ? j : ii;
-        const uint32_t g = (uint32_t)gamma;
-        const bool left_leaf = lo == gamma, right_leaf = hi == gamma + 1;
+        const uint32_t g = toward(i, s, d) - (d < 0 ? 1u : 0u);
+        const uint32_t lo = i < j ? i : j, hi = i < j ? j : i;
+        const bool left_leaf = lo == g, right_leaf = hi == g + 1;
         left[i] = left_leaf ? (g | kLeafFlag) : g;
         right[i] = right_leaf ? ((g + 1) | kLeafFlag) : g + 1;
-        first[i] = (uint32_t)lo;
-        last[i] = (uint32_t)hi;
+        first[i] = lo;
+        last[i] = hi;
         if (left_leaf) leaf_parent[g] = i;
         else node_parent[g] = i;
         if (right_leaf) leaf_parent[g + 1] = i;
