@@ -48,15 +48,23 @@ __device__ __forceinline__ int delta(const uint32_t* __restrict__ codes, uint32_
 
 // delta(i, j) > m, for m in [-1, 63], without counting the prefix: the keys
 // share more than m leading bits exactly when their 64-bit XOR, (code xor)
-// << 32 | (position xor), is below 2^(63 - m).
+// << 32 | (position xor), is below 2^(63 - m), i.e. has no bit set under the
+// masks of Above(m) (high word: code xor; low word: position xor).
+struct Above {
+    uint32_t hmask, lmask;
+    __device__ __forceinline__ explicit Above(int m)
+    {
+        const int s = 63 - m;  // 0..64
+        hmask = s >= 64 ? 0u : s >= 32 ? ~0u << (s - 32) : ~0u;
+        lmask = s >= 32 ? 0u : ~0u << s;
+    }
+};
+
 __device__ __forceinline__ bool shares_more(const uint32_t* __restrict__ codes, uint32_t n, uint32_t i,
-                                            uint32_t ci, uint32_t j, int m)
+                                            uint32_t ci, uint32_t j, Above a)
 {
     if (j >= n) return false;
-    const uint32_t hx = ci ^ __ldg(codes + j);
-    const int s = 63 - m;  // 0..64
-    if (s >= 32) return s >= 64 || (hx >> (s - 32)) == 0u;
-    return hx == 0u && ((i ^ j) >> s) == 0u;
+    return (((ci ^ __ldg(codes + j)) & a.hmask) | ((i ^ j) & a.lmask)) == 0u;
 }
 
 __global__ void __launch_bounds__(256) k_lbvh_build(const uint32_t* __restrict__ codes, uint32_t n,
@@ -70,21 +78,21 @@ __global__ void __launch_bounds__(256) k_lbvh_build(const uint32_t* __restrict__
         const uint32_t ci = __ldg(codes + i);
         // Direction of the range: towards the neighbour sharing the longer prefix.
         const int d = (delta(codes, n, i, ci, i + 1) - delta(codes, n, i, ci, i - 1)) >= 0 ? 1 : -1;
-        // The far end: every key in the range shares more than delta_min with key(i).
-        const int delta_min = delta(codes, n, i, ci, toward(i, 1, -d));
+        // The far end: every key in the range shares more than delta(i, i - d) bits with key(i).
+        const Above far(delta(codes, n, i, ci, toward(i, 1, -d)));
         uint32_t lmax = 2;
-        while (shares_more(codes, n, i, ci, toward(i, lmax, d), delta_min)) lmax <<= 1;
+        while (shares_more(codes, n, i, ci, toward(i, lmax, d), far)) lmax <<= 1;
         uint32_t l = 0;
         for (uint32_t t = lmax >> 1; t >= 1; t >>= 1)
-            if (shares_more(codes, n, i, ci, toward(i, l + t, d), delta_min)) l += t;
+            if (shares_more(codes, n, i, ci, toward(i, l + t, d), far)) l += t;
         const uint32_t j = toward(i, l, d);
         // The split: the last key (from i towards j) sharing more than the
         // node's own prefix with key(i).
-        const int delta_node = delta(codes, n, i, ci, j);
+        const Above split(delta(codes, n, i, ci, j));
         uint32_t s = 0, t = l;
         do {
             t = (t + 1) >> 1;
-            if (shares_more(codes, n, i, ci, toward(i, s + t, d), delta_node)) s += t;
+            if (shares_more(codes, n, i, ci, toward(i, s + t, d), split)) s += t;
         } while (t > 1);
         const uint32_t g = toward(i, s, d) - (d < 0 ? 1u : 0u);
         const uint32_t lo = i < j ? i : j, hi = i < j ? j : i;
