@@ -158,14 +158,17 @@ def ncu_traffic(kind: str, workload: str):
 def link_times(host_in, host_out, dev_buf, dev) -> dict:
     """The host link on this machine, for reading e2e: one step's input copied
     in alone, its result copied out alone, and both at once on two streams
-    (best of 3, CUDA events).  The pipelined e2e step cannot beat `both_ms`."""
+    (3 of each, CUDA events; `*_ms` the fastest, `*_slowest_ms` the slowest).
+    The pipelined e2e step cannot beat `both_ms`; single copies on these
+    hosts now and then stall for tens of milliseconds, which the slowest
+    samples show."""
     import torch
     nbytes = host_in.numel() * host_in.element_size()
     d_in = dev_buf[:nbytes].view(host_in.dtype)
     d_out = dev_buf[nbytes:2 * nbytes].view(host_in.dtype)
     side = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
 
-    def best(fn):
+    def samples(fn):
         ms = []
         for _ in range(3):
             cur = torch.cuda.current_stream(dev)
@@ -175,7 +178,7 @@ def link_times(host_in, host_out, dev_buf, dev) -> dict:
             e1.record(cur)
             torch.cuda.synchronize(dev)
             ms.append(e0.elapsed_time(e1))
-        return round(min(ms), 3)
+        return ms
 
     def both(cur):
         for sd in side:
@@ -186,10 +189,14 @@ def link_times(host_in, host_out, dev_buf, dev) -> dict:
             host_out.copy_(d_out, non_blocking=True)
         for sd in side:
             cur.wait_stream(sd)
-    return {"bytes": nbytes,
-            "h2d_ms": best(lambda cur: d_in.copy_(host_in, non_blocking=True)),
-            "d2h_ms": best(lambda cur: host_out.copy_(d_out, non_blocking=True)),
-            "both_ms": best(both)}
+    out = {"bytes": nbytes}
+    for name, fn in (("h2d", lambda cur: d_in.copy_(host_in, non_blocking=True)),
+                     ("d2h", lambda cur: host_out.copy_(d_out, non_blocking=True)),
+                     ("both", both)):
+        ms = samples(fn)
+        out[f"{name}_ms"] = round(min(ms), 3)
+        out[f"{name}_slowest_ms"] = round(max(ms), 3)
+    return out
 
 
 class ClockSampler:
