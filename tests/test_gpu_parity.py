@@ -153,6 +153,18 @@ def test_keys_only_mixed_entropy_chunks(kt, descending):
     assert np.array_equal(got_k, oracle.sort(kt, keys, None, 0, bits, descending=descending)[0])
 
 
+@pytest.mark.parametrize("kt,vals,bytes_per_key", [("u32", False, 4), ("u32", True, 8), ("u64", False, 8),
+                                                   ("u64", True, 12), ("u16", False, 4)])
+def test_chained_scan_tile_width_boundary(kt, vals, bytes_per_key):
+    # The chained scan runs 256-thread tiles below 4 MiB of keys and values
+    # (16-bit keys counted as 4 bytes) and 512-thread tiles from there: sort
+    # just below and at the boundary.
+    edge = (4 << 20) // bytes_per_key
+    for i, n in enumerate((edge - 1, edge, edge + 1)):
+        keys = synth.u16_uniform(n, 60 + i) if kt == "u16" else gen_keys(kt, n, 60 + i)
+        check(kt, keys, synth.iota_u32(n) if vals else None, 0, rs.KEY_BITS[kt], algo="onesweep")
+
+
 def test_many_tiles_onesweep_lookback():
     # > 256 tiles per pass, uneven tail: exercises long look-back chains
     n = (1 << 22) + 12345
