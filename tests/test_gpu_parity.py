@@ -143,7 +143,7 @@ def test_float_specials_and_signed_zero():
 def test_keys_only_mixed_entropy_chunks(kt, descending):
     # Keys-only reduce-then-scan over chunks of different digit skew (uniform,
     # AND of 4, 8 distinct values, one repeated key, uniform), so the CTAs of
-    # one pass see different digit mixes and rank with different match widths.
+    # one pass see very different digit mixes.
     m = 300_001
     raw = np.concatenate([synth.u32_uniform(m, 41), synth.u32_and4(m, 42), synth.u32_bits(m, 1, 3),
                           np.full(m, 0x80000001, np.uint32), synth.u32_uniform(m + 777, 43)])
@@ -151,6 +151,23 @@ def test_keys_only_mixed_entropy_chunks(kt, descending):
     bits = 16 if kt == "u16" else 32
     got_k, _ = gpu_sort(kt, keys, None, 0, bits, algo="reduce_scan", descending=descending)
     assert np.array_equal(got_k, oracle.sort(kt, keys, None, 0, bits, descending=descending)[0])
+
+
+@pytest.mark.parametrize("dist", ["uniform", "and4", "eight_values", "low_byte_only"])
+@pytest.mark.parametrize("kt", ["u32", "f32", "u16"])
+def test_keys_only_digit_skews(dist, kt):
+    # Keys-only reduce-then-scan (the staged tiles) over uniform digits, AND-of-4
+    # skew, eight distinct keys and keys whose upper bytes are all zero, both
+    # orders.
+    n = (1 << 20) + 77
+    raw = {"uniform": synth.u32_uniform(n, 70), "and4": synth.u32_and4(n, 71),
+           "eight_values": synth.u32_bits(n, 72, 3), "low_byte_only": synth.u32_uniform(n, 73) & np.uint32(0xFF)}[dist]
+    keys = (raw >> np.uint32(16)).astype(np.uint16) if kt == "u16" and dist in ("uniform", "and4") \
+        else raw.astype(np.uint16) if kt == "u16" else raw
+    bits = rs.KEY_BITS[kt]
+    for descending in (False, True):
+        got_k, _ = gpu_sort(kt, keys, None, 0, bits, algo="reduce_scan", descending=descending)
+        assert np.array_equal(got_k, oracle.sort(kt, keys, None, 0, bits, descending=descending)[0])
 
 
 @pytest.mark.parametrize("kt,vals,bytes_per_key", [("u32", False, 4), ("u32", True, 8), ("u64", False, 8),
